@@ -1,0 +1,59 @@
+"""Plant plausible mistakes in a copy of the oracle (on the CPU) and check that the pins
+catch every one of them: a pin suite that a dropped term, a wrong sign or index or a
+transposed operand passes would prove nothing."""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+import oracle_pins as pins
+
+SRC = open(os.path.join(os.path.dirname(oracle.__file__), "ref_attn.c")).read()
+
+MUTATIONS = {
+    "causal_excludes_self": ("int hi = causal ? p : L - 1;", "int hi = causal ? p - 1 : L - 1;"),
+    "noncausal_drops_last": ("int hi = causal ? p : L - 1;", "int hi = causal ? p : L - 2;"),
+    "window_one_short": ("lo = p - window_left > 0 ? p - window_left : 0;",
+                          "lo = p - window_left + 1 > 0 ? p - window_left + 1 : 0;"),
+    "window_ignored": ("if (window_left >= 0) lo", "if (window_left >= 1000000) lo"),
+    "gqa_modulo_mapping": ("int hk = h / group;", "int hk = h % num_kv_heads;"),
+    "k_v_swapped": ("size_t ko = cache_offset(page, 0, slot, hk,", "size_t ko = cache_offset(page, 1, slot, hk,"),
+    "no_sm_scale": ("s[j] = sm_scale * dot;", "s[j] = dot;"),
+    "unnormalised": ("float w = s[j] / l;", "float w = s[j];"),
+    "lse_log2": ("m + logf(l)", "m + log2f(l)"),
+    "lse_without_max": ("m + logf(l)", "logf(l)"),
+    "slot_shift": ("int slot = p % page_size;\n            for (int hk",
+                   "int slot = (p + 1) % page_size;\n            for (int hk"),
+    "page_index_off_by_one": ("int64_t page = kv_indices[kv_indptr[r] + p / page_size];\n            if (page < 0 || page >= max_pages) { free",
+                              "int64_t page = kv_indices[kv_indptr[r] + (p + 1) / page_size];\n            if (page < 0 || page >= max_pages) { free"),
+    "row_length_ignores_last_page": ("return (npages - 1) * page_size + last_page_len[r];",
+                                     "return npages * page_size;"),
+    "append_one_late": ("int p = c + i;\n            int64_t page", "int p = c + i + 1;\n            int64_t page"),
+    "append_v_into_k": ("memcpy(kv_layer + vo,", "memcpy(kv_layer + ko,"),
+    "query_token_of_row_start": ("int t = qo_indptr[r] + i;\n            int p = c + i;\n            int hi",
+                                 "int t = qo_indptr[r];\n            int p = c + i;\n            int hi"),
+}
+
+
+def _build(tmp_path, name, src):
+    c = tmp_path / f"{name}.c"
+    so = tmp_path / f"{name}.so"
+    c.write_text(src)
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", str(c), "-o", str(so),
+                    "-lm"], check=True)
+    return oracle.load(str(so))
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_mutant_is_caught(name, tmp_path):
+    old, new = MUTATIONS[name]
+    assert SRC.count(old) == 1, f"mutation anchor for {name} not unique"
+    lib = _build(tmp_path, name, SRC.replace(old, new))
+    caught = []
+    for pin in pins.ALL_PINS:
+        try:
+            pin(lib=lib)
+        except (AssertionError, ValueError, IndexError) as e:
+            caught.append(pin.__name__)
+    assert caught, f"no pin caught mutation {name}"
