@@ -1,0 +1,223 @@
+/*
+ * pkv: batched GQA attention over a paged bf16 KV cache, for GB300 (sm_103a).
+ *
+ * C ABI.  Plain pointers and sizes only.  Device pointers are CUDA device
+ * addresses on the current device; host pointers are ordinary process memory.
+ * The caller owns every device buffer (q, k/v, out, lse, the KV layer slice, the
+ * workspace).  The library allocates no device memory; it owns the opaque handle
+ * and the handle's page-locked host staging ring.
+ *
+ * Cache layout (mstar.engine.resources.attn.wrappers, module docstring): the full
+ * cache is [num_layers, max_pages, 2, page_size, num_kv_heads, head_dim] bf16; every
+ * call here takes ONE layer slice [max_pages, 2, page_size, num_kv_heads, head_dim]
+ * (index 0 of the "2" axis = K, 1 = V), contiguous, 16-byte aligned.
+ *
+ * Index arrays (mstar.engine.resources.kv.plan, PagedIndptrs): int32
+ *   qo_indptr[batch+1]      new-token offsets of each row into q / out
+ *   paged_kv_indptr[batch+1] page offsets of each row into paged_kv_indices
+ *   paged_kv_indices[nnz]   page ids, in position order within a row
+ *   paged_kv_last_page_len[batch] slots filled in each row's last page, 1..page_size
+ * They describe the cache AFTER this step's append (the layer writes its K/V before
+ * attention runs: DenseAttentionManager.requires_kv_write), so row r holds
+ *   L_r = (pages_r - 1) * page_size + last_page_len[r] tokens, of which the last
+ *   n_r = qo_indptr[r+1] - qo_indptr[r] are this step's new tokens.
+ *
+ * Attention (the softmax definition the wrappers compute): new token i of row r sits
+ * at position p = L_r - n_r + i; q head h reads kv head h / (num_qo_heads/num_kv_heads);
+ * it sees keys j with lo <= j <= p (causal) or lo <= j <= L_r - 1 (non-causal), where
+ * lo = max(0, p - window_left) if window_left >= 0, else 0 (FlashInferPrefillWrapper.plan:
+ * window_left is the number of preceding positions a query sees, -1 unbounded);
+ *   out = softmax(sm_scale * q K^T) V (bf16), lse = natural-log log-sum-exp (fp32).
+ *
+ * Call order for one step:  pkv_plan (host)  ->  per layer: pkv_kv_append, then
+ * pkv_run_decode / pkv_run_prefill / pkv_run_mixed.  One plan serves every layer
+ * until the next plan on that workspace (DensePlan: "once per step and read by each
+ * layer run").  run and append calls allocate nothing and never synchronise the host.
+ *
+ * Errors: every function returns a pkv_status; validation happens on the host before
+ * any launch; pkv_last_error() explains the last failure.  Kernels never trap: a
+ * device-side wait that exceeds its iteration limit records an error word in the
+ * workspace, which pkv_check_device_error() reads.
+ *
+ * Threading: one handle per issuing thread.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct pkv_handle_s *pkv_handle_t;
+typedef void *pkv_stream_t; /* a cudaStream_t; NULL = the legacy default stream */
+
+typedef enum {
+    PKV_OK = 0,
+    PKV_ERR_INVALID = 1,               /* malformed arguments or index arrays */
+    PKV_ERR_UNSUPPORTED = 2,           /* a shape this build's kernels do not compute */
+    PKV_ERR_WORKSPACE = 3,             /* workspace too small: pkv_last_error names the bytes */
+    PKV_ERR_TOO_MANY_PREFILL_ROWS = 4, /* mixed plan with more prompt rows than max_prefill_rows */
+    PKV_ERR_NOT_PLANNED = 5,           /* run/append without a matching plan on that workspace */
+    PKV_ERR_CUDA = 6,                  /* a CUDA runtime/driver call failed */
+    PKV_ERR_DEVICE = 7                 /* a kernel recorded a device-side error (wait limit hit) */
+} pkv_status;
+
+enum { PKV_MODE_DECODE = 0, PKV_MODE_PREFILL = 1, PKV_MODE_MIXED = 2 };
+
+/*
+ * Static configuration, fixed for the life of a handle (the wrappers' constructor
+ * arguments: FlashInferDecodeWrapper / FlashInferPrefillWrapper / FlashInferMixedWrapper).
+ *   num_qo_heads, num_kv_heads, head_dim, page_size: shape of q and of the cache.
+ *   max_batch:        most rows a plan may have.
+ *   max_total_tokens: most new tokens a plan may have (prefill and mixed).
+ *   max_num_pages:    most entries paged_kv_indices may have.
+ *   num_cache_pages:  pages in one layer slice (its first dimension); every page id
+ *                     must be below it.
+ *   max_prefill_rows: mixed only: most prompt rows (rows with >= 2 new tokens).
+ *   sm_count:         SMs the work split targets; 0 = query the current device.
+ *   sink_page:        mixed only: a caller-reserved page id holding finite values,
+ *                     read (one token) by every non-decode row of the decode pass;
+ *                     -1 when no mixed plans are made.
+ */
+typedef struct {
+    int num_qo_heads;
+    int num_kv_heads;
+    int head_dim;
+    int page_size;
+    int max_batch;
+    int max_total_tokens;
+    int max_num_pages;
+    int num_cache_pages;
+    int max_prefill_rows;
+    int sm_count;
+    int sink_page;
+} pkv_config;
+
+/*
+ * Create a handle.  Host-only apart from the device query when sm_count == 0.
+ * Returns PKV_ERR_UNSUPPORTED unless head_dim is 64 or 128, page_size is 16,
+ * num_qo_heads is a multiple of num_kv_heads with a group of 1..16, and
+ * num_kv_heads <= 16 (check_flashinfer_head_dim: the pages' kernels likewise reject
+ * a head_dim they do not compute exactly).  PKV_ERR_INVALID on non-positive sizes.
+ * *out is set only on PKV_OK.
+ */
+pkv_status pkv_create(const pkv_config *cfg, pkv_handle_t *out);
+
+/* Release the handle and its pinned staging (waits for that staging's copies). */
+void pkv_destroy(pkv_handle_t h);
+
+/* Message for the last failure on this handle (never NULL; "" when none).  With
+ * h == NULL, the message of the last failed pkv_create on this thread. */
+const char *pkv_last_error(pkv_handle_t h);
+
+/*
+ * Bytes of device workspace a plan of `mode` needs at the handle's static maxima
+ * (the worst case: mstar.engine.resources.attn.workspace, Workspace: what a plan
+ * needs depends on rows, segments, heads and the SM count).  Host-only.
+ */
+pkv_status pkv_workspace_size(pkv_handle_t h, int mode, size_t *bytes);
+
+/*
+ * Plan a step (FlashInferDecodeWrapper.plan / FlashInferPrefillWrapper.plan /
+ * FlashInferMixedWrapper.plan).  All index arrays are HOST int32 pointers (the pages
+ * prefer CPU inputs so planning never waits on the device).  The planner validates
+ * them, derives the KV write locations, splits the attention into work tiles sized to
+ * the SM count (split-KV partials live in the workspace), for mode MIXED classifies
+ * rows and builds the prompt-token permutation and the sink routing, stages the plan
+ * in page-locked memory and copies it into `workspace` with one async H2D on `stream`.
+ *   mode          PKV_MODE_DECODE: qo_indptr may be NULL (row r's query is token r);
+ *                 PKV_MODE_PREFILL / PKV_MODE_MIXED: qo_indptr required.
+ *   causal        prefill and mixed (the prefill pass); decode is always "sees its row".
+ *   window_left   -1 unbounded, else >= 0.
+ *   sm_scale      0 selects 1/sqrt(head_dim).
+ *   workspace     device buffer of workspace_bytes (>= pkv_workspace_size for the
+ *                 plan actually made; 256-byte aligned).  A too-small workspace returns
+ *                 PKV_ERR_WORKSPACE and pkv_last_error states the bytes required.
+ * Host staging is a ring of two page-locked sets fenced by CUDA events
+ * (PinnedIndexRing), so a plan may be issued while the previous step still runs.
+ */
+pkv_status pkv_plan(pkv_handle_t h, int mode, const int32_t *qo_indptr, const int32_t *paged_kv_indptr,
+                    const int32_t *paged_kv_indices, const int32_t *paged_kv_last_page_len, int batch,
+                    int causal, int window_left, float sm_scale, void *workspace, size_t workspace_bytes,
+                    pkv_stream_t stream);
+
+/*
+ * Last-page KV append (the write locations the plan computed; the KVManager's write
+ * before attention).  k, v: device bf16 [T, num_kv_heads, head_dim], T = the planned
+ * step's new tokens (decode: batch).  kv_layer: device layer slice, written in place
+ * at (page, slot) of each new token; nothing else in the slice is touched.
+ */
+pkv_status pkv_kv_append(pkv_handle_t h, const void *k, const void *v, void *kv_layer, void *workspace,
+                         pkv_stream_t stream);
+
+/*
+ * Batched decode (FlashInferDecodeWrapper.run).  q: device bf16 [batch, Hq, D];
+ * out: device bf16 [batch, Hq, D]; lse: device fp32 [batch, Hq] or NULL.
+ */
+pkv_status pkv_run_decode(pkv_handle_t h, const void *q, const void *kv_layer, void *out, float *lse,
+                          void *workspace, pkv_stream_t stream);
+
+/*
+ * Ragged prefill over a cached prefix (FlashInferPrefillWrapper.run).  q, out: device
+ * bf16 [T, Hq, D] in qo_indptr order; lse: device fp32 [T, Hq] or NULL.
+ */
+pkv_status pkv_run_prefill(pkv_handle_t h, const void *q, const void *kv_layer, void *out, float *lse,
+                           void *workspace, pkv_stream_t stream);
+
+/*
+ * Mixed step (FlashInferMixedWrapper.run): the decode pass over every row of the
+ * plan (non-decode rows read one token of sink_page, their result is dropped) and
+ * the prefill pass over the prompt rows (at most max_prefill_rows, padded with empty
+ * rows).  q, out: device bf16 [T, Hq, D] in the original qo_indptr order; lse: device
+ * fp32 [T, Hq] or NULL.
+ */
+pkv_status pkv_run_mixed(pkv_handle_t h, const void *q, const void *kv_layer, void *out, float *lse,
+                         void *workspace, pkv_stream_t stream);
+
+/*
+ * Read and clear the workspace's device error word (synchronises `stream`).
+ * PKV_OK when no kernel recorded an error since the last plan on it.
+ */
+pkv_status pkv_check_device_error(pkv_handle_t h, void *workspace, pkv_stream_t stream, int *code);
+
+/* ---- host-only planning queries (no CUDA call; usable on a machine without a GPU) ---- */
+
+/*
+ * KV write locations of a step (FlashInferDecodeWrapper.plan: "compute KV write
+ * locations"; KVPlanOutput.decode_pages / decode_offsets): for every new token t,
+ * pages[t] and slots[t].  Host arrays of the step's token count.
+ */
+pkv_status pkv_append_slots(int page_size, const int32_t *qo_indptr, const int32_t *paged_kv_indptr,
+                            const int32_t *paged_kv_indices, const int32_t *paged_kv_last_page_len, int batch,
+                            int32_t *pages, int32_t *slots);
+
+/*
+ * The mixed step's two plans (FlashInferMixedWrapper): is_decode[batch], prompt_rows
+ * [max_prefill_rows] (-1 padding), perm[T] (perm[k] = original token of permuted token
+ * k: prompt tokens first in row order, then the rest in order), pf_qo_indptr
+ * [max_prefill_rows+1], the decode pass's dec_kv_indptr[batch+1], dec_kv_indices
+ * [<= nnz + batch], dec_last_page_len[batch], dec_q_token[batch], dec_out_token[batch]
+ * (-1 = dropped).  *dec_nnz receives the length of dec_kv_indices.
+ */
+pkv_status pkv_mixed_layout(const int32_t *qo_indptr, const int32_t *paged_kv_indptr,
+                            const int32_t *paged_kv_indices, const int32_t *paged_kv_last_page_len, int batch,
+                            int max_prefill_rows, int sink_page, int32_t *is_decode, int32_t *prompt_rows,
+                            int32_t *perm, int32_t *pf_qo_indptr, int32_t *dec_kv_indptr,
+                            int32_t *dec_kv_indices, int32_t *dec_last_page_len, int32_t *dec_q_token,
+                            int32_t *dec_out_token, int *dec_nnz);
+
+/*
+ * The decode work split the plan would make: tiles[k] = {row, first visible page,
+ * page count, partial slot or -1 for a direct write, cta}.  *num_tiles in: capacity
+ * (tiles holds 5 * capacity ints), out: tiles written.  *num_ctas receives the grid.
+ */
+pkv_status pkv_decode_split(pkv_handle_t h, const int32_t *paged_kv_indptr, const int32_t *paged_kv_last_page_len,
+                            int batch, int window_left, int32_t *tiles, int *num_tiles, int *num_ctas);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PKV_H */

@@ -1,0 +1,421 @@
+// Batched paged decode with split-KV, the split-KV merge, and the last-page append.
+//
+// Decode (FlashInferDecodeWrapper.run; mstar.engine.resources.attn.wrappers): every row
+// has one query token; q head h attends, through kv head h / g, to the row's visible
+// positions [lo, L-1] (lo = max(0, L-1-window_left), or 0), o = softmax(sm_scale q K^T) V,
+// lse = ln sum exp.
+//
+// Design for GB300:
+//  * A persistent grid of one CTA per SM.  The planner hands each CTA a contiguous run
+//    of the batch's visible pages (balanced to +-1 page); a row cut by a CTA boundary
+//    writes an fp32 partial (o normalised, lse) into the workspace, merged afterwards.
+//  * One page of ALL kv heads is contiguous in the cache (K: page_size x Hkv x D, then V),
+//    so a CTA streams whole pages: one producer thread issues 2 x D/64 TMA boxes per page
+//    (K and V, 64-column halves, 128-byte swizzle) into a ring of stages, completion on an
+//    mbarrier; consumers release a stage through a second mbarrier.
+//  * One consumer warp per kv head.  The g query heads of the group are the M dimension of
+//    a 16x8x16 bf16 tensor-core MMA (padded to 16 rows); keys are N for QK^T and K for PV.
+//    Online softmax in the exp2 domain with quad shuffles.
+//  * Slots past the row's end in its last page are zeroed in shared memory before PV
+//    (their scores are masked to -inf; zeroing V keeps 0 * NaN out of the MMA).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "launch.h"
+#include "plan.h"
+#include "ptx.cuh"
+
+namespace pkv {
+namespace dev {
+
+struct DecodeArgs {
+    const __nv_bfloat16 *q;
+    __nv_bfloat16 *out;
+    float *lse;
+    const DecodeTile *tiles;
+    const int32_t *cta_ptr;
+    const int32_t *pages;
+    float *part_o;
+    float *part_lse;
+    int *err;
+    int num_qo_heads;
+    int num_kv_heads;
+    int page_size;
+    int stages;
+    uint32_t stage_bytes;
+    uint32_t box_bytes;
+    float scale_log2;  // sm_scale * log2(e)
+};
+
+constexpr float kLn2 = 0.6931471805599453f;
+
+template <int D, int G>
+__global__ void __launch_bounds__(9 * 32, 1)
+    decode_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeArgs a) {
+    constexpr int KS = D / 16;  // k-steps of QK^T
+    constexpr int NT = D / 8;   // 8-wide output column tiles
+    constexpr int HALVES = D / 64;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)a.stages * a.stage_bytes);
+    uint64_t *empty = full + a.stages;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int Hkv = a.num_kv_heads;
+    const int P = a.page_size;
+    const int t_begin = a.cta_ptr[blockIdx.x];
+    const int t_end = a.cta_ptr[blockIdx.x + 1];
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < a.stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], Hkv);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == Hkv) {
+        // ---------------- producer ----------------
+        if (lane == 0) {
+            prefetch_tmap(&tmap);
+            uint32_t it = 0;
+            bool ok = true;
+            for (int ti = t_begin; ti < t_end && ok; ++ti) {
+                const DecodeTile t = a.tiles[ti];
+                for (int pi = t.page_begin; pi < t.page_begin + t.page_count; ++pi, ++it) {
+                    const int s = it % a.stages;
+                    const uint32_t use = it / a.stages;
+                    if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, a.err, kErrWaitEmpty)) {
+                        ok = false;
+                        break;
+                    }
+                    const int page = a.pages[t.kv_base + pi];
+                    uint8_t *st = smem + (size_t)s * a.stage_bytes;
+                    mbar_arrive_expect_tx(&full[s], a.stage_bytes);
+#pragma unroll
+                    for (int kv = 0; kv < 2; ++kv)
+#pragma unroll
+                        for (int h = 0; h < HALVES; ++h)
+                            tma_load_3d(st + (kv * HALVES + h) * a.box_bytes, &tmap, &full[s], h * 64,
+                                        (page * 2 + kv) * P, 0);
+                }
+            }
+            // Drain: every stage issued must have been consumed before the CTA exits.
+            const uint32_t issued = it;
+            for (uint32_t k = issued > (uint32_t)a.stages ? issued - a.stages : 0; k < issued; ++k) {
+                const int s = k % a.stages;
+                if (!mbar_wait(&empty[s], (k / a.stages) & 1, a.err, kErrWaitDrain)) break;
+            }
+        }
+        return;
+    }
+    if (warp >= Hkv) return;
+
+    // ---------------- consumers: warp = kv head ----------------
+    const int hk = warp;
+    const int gid = lane >> 2;   // row of the MMA fragment (query head within the group)
+    const int tid4 = lane & 3;
+    const int Hq = a.num_qo_heads;
+    // ldmatrix lane roles
+    const int k_tok = (lane & 7) + ((lane >> 4) << 3);
+    const int k_chk = (lane >> 3) & 1;
+    const int v_tok = (lane & 7) + (((lane >> 3) & 1) << 3);
+    const int v_chk = lane >> 4;
+
+    uint32_t it = 0;
+    for (int ti = t_begin; ti < t_end; ++ti) {
+        const DecodeTile t = a.tiles[ti];
+        // Query fragments: rows = the g heads of this kv head (rows >= G are zero).
+        uint32_t qa[KS][4];
+        {
+            const __nv_bfloat16 *qrow = a.q + ((size_t)t.q_token * Hq + (size_t)hk * G) * D;
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                const int c0 = ks * 16 + tid4 * 2;
+                qa[ks][0] = gid < G ? *reinterpret_cast<const uint32_t *>(qrow + (size_t)gid * D + c0) : 0u;
+                qa[ks][2] = gid < G ? *reinterpret_cast<const uint32_t *>(qrow + (size_t)gid * D + c0 + 8) : 0u;
+                qa[ks][1] = gid + 8 < G ? *reinterpret_cast<const uint32_t *>(qrow + (size_t)(gid + 8) * D + c0) : 0u;
+                qa[ks][3] =
+                    gid + 8 < G ? *reinterpret_cast<const uint32_t *>(qrow + (size_t)(gid + 8) * D + c0 + 8) : 0u;
+            }
+        }
+        float acc[NT][4];
+#pragma unroll
+        for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+        for (int pi = t.page_begin; pi < t.page_begin + t.page_count; ++pi, ++it) {
+            const int s = it % a.stages;
+            if (!mbar_wait(&full[s], (it / a.stages) & 1, a.err, kErrWaitFull)) return;
+            uint8_t *st = smem + (size_t)s * a.stage_bytes;
+            const uint32_t kbase = smem_u32(st);
+            const uint32_t vbase = kbase + HALVES * a.box_bytes;
+            const int pos0 = pi * P;
+            const int nvalid = t.length - pos0;  // slots holding tokens of this row
+            if (nvalid < P) {
+                // zero V rows past the row's end (stale or poisoned slots)
+                const int nz = (P - nvalid) * (D / 8);
+                for (int i = lane; i < nz; i += 32) {
+                    const int slot = nvalid + i / (D / 8);
+                    const int chunk = i % (D / 8);
+                    const int row = hk * P + slot;
+                    *reinterpret_cast<uint4 *>(st + HALVES * a.box_bytes + (chunk >> 3) * a.box_bytes +
+                                               swz128(row, chunk & 7)) = make_uint4(0, 0, 0, 0);
+                }
+                __syncwarp();
+            }
+            // S = Q K^T over the page's 16 slots: two n-tiles of 8 keys.
+            float sc[2][4];
+#pragma unroll
+            for (int n = 0; n < 2; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                const int chunk = ks * 2 + k_chk;
+                const uint32_t addr = kbase + (chunk >> 3) * a.box_bytes + swz128(hk * P + k_tok, chunk & 7);
+                uint32_t b0, b1, b2, b3;
+                ldmatrix_x4(addr, b0, b1, b2, b3);
+                mma_bf16_16816(sc[0], qa[ks], b0, b1);
+                mma_bf16_16816(sc[1], qa[ks], b2, b3);
+            }
+            // mask + online softmax (exp2 domain)
+            float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int pos = pos0 + n * 8 + tid4 * 2 + e;
+                    const bool vis = pos >= t.lo && pos < t.length;
+                    sc[n][e] = vis ? sc[n][e] * a.scale_log2 : -INFINITY;
+                    sc[n][e + 2] = vis ? sc[n][e + 2] * a.scale_log2 : -INFINITY;
+                    mx0 = fmaxf(mx0, sc[n][e]);
+                    mx1 = fmaxf(mx1, sc[n][e + 2]);
+                }
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+            const float ref0 = mn0 == -INFINITY ? 0.f : mn0;
+            const float ref1 = mn1 == -INFINITY ? 0.f : mn1;
+            const float al0 = fast_exp2(m0 - ref0), al1 = fast_exp2(m1 - ref1);
+            m0 = mn0;
+            m1 = mn1;
+            float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    sc[n][e] = fast_exp2(sc[n][e] - ref0);
+                    sc[n][e + 2] = fast_exp2(sc[n][e + 2] - ref1);
+                    ps0 += sc[n][e];
+                    ps1 += sc[n][e + 2];
+                }
+            l0 = l0 * al0 + ps0;
+            l1 = l1 * al1 + ps1;
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                acc[n][0] *= al0;
+                acc[n][1] *= al0;
+                acc[n][2] *= al1;
+                acc[n][3] *= al1;
+            }
+            uint32_t pa[4];
+            pa[0] = pack_bf16(sc[0][0], sc[0][1]);
+            pa[1] = pack_bf16(sc[0][2], sc[0][3]);
+            pa[2] = pack_bf16(sc[1][0], sc[1][1]);
+            pa[3] = pack_bf16(sc[1][2], sc[1][3]);
+            // O += P V
+#pragma unroll
+            for (int dj = 0; dj < D / 16; ++dj) {
+                const int chunk = dj * 2 + v_chk;
+                const uint32_t addr = vbase + (chunk >> 3) * a.box_bytes + swz128(hk * P + v_tok, chunk & 7);
+                uint32_t b0, b1, b2, b3;
+                ldmatrix_x4_trans(addr, b0, b1, b2, b3);
+                mma_bf16_16816(acc[2 * dj], pa, b0, b1);
+                mma_bf16_16816(acc[2 * dj + 1], pa, b2, b3);
+            }
+            if (nvalid < P) fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+        }
+
+        // finalise the piece
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+        const float inv0 = 1.f / l0, inv1 = 1.f / l1;
+        const float lse0 = (m0 + __log2f(l0)) * kLn2;
+        const float lse1 = (m1 + __log2f(l1)) * kLn2;
+        const int h0 = hk * G + gid, h1 = hk * G + gid + 8;
+        if (t.partial < 0) {
+            if (t.out_token >= 0) {
+                __nv_bfloat16 *o = a.out + (size_t)t.out_token * Hq * D;
+#pragma unroll
+                for (int n = 0; n < NT; ++n) {
+                    const int c = n * 8 + tid4 * 2;
+                    if (gid < G)
+                        *reinterpret_cast<uint32_t *>(o + (size_t)h0 * D + c) =
+                            pack_bf16(acc[n][0] * inv0, acc[n][1] * inv0);
+                    if (gid + 8 < G)
+                        *reinterpret_cast<uint32_t *>(o + (size_t)h1 * D + c) =
+                            pack_bf16(acc[n][2] * inv1, acc[n][3] * inv1);
+                }
+                if (a.lse && tid4 == 0) {
+                    if (gid < G) a.lse[(size_t)t.out_token * Hq + h0] = lse0;
+                    if (gid + 8 < G) a.lse[(size_t)t.out_token * Hq + h1] = lse1;
+                }
+            }
+        } else {
+            float *po = a.part_o + (size_t)t.partial * Hq * D;
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                const int c = n * 8 + tid4 * 2;
+                if (gid < G)
+                    *reinterpret_cast<float2 *>(po + (size_t)h0 * D + c) = make_float2(acc[n][0] * inv0, acc[n][1] * inv0);
+                if (gid + 8 < G)
+                    *reinterpret_cast<float2 *>(po + (size_t)h1 * D + c) = make_float2(acc[n][2] * inv1, acc[n][3] * inv1);
+            }
+            if (tid4 == 0) {
+                if (gid < G) a.part_lse[(size_t)t.partial * Hq + h0] = lse0;
+                if (gid + 8 < G) a.part_lse[(size_t)t.partial * Hq + h1] = lse1;
+            }
+        }
+    }
+}
+
+// Merge the split-KV partials of each cut row: with w_j = exp(lse_j - max lse),
+// o = sum_j w_j o_j / sum_j w_j and lse = max lse + ln sum_j w_j.
+__global__ void __launch_bounds__(256) merge_kernel(const MergeRow *rows, const float *part_o, const float *part_lse,
+                                                    __nv_bfloat16 *out, float *lse, int Hq, int D) {
+    const MergeRow mr = rows[blockIdx.x];
+    if (mr.out_token < 0) return;
+    const int per_head = D / 4;
+    for (int e = threadIdx.x; e < Hq * per_head; e += blockDim.x) {
+        const int h = e / per_head;
+        const int c = (e % per_head) * 4;
+        float M = -INFINITY;
+        for (int j = 0; j < mr.count; ++j) M = fmaxf(M, part_lse[(size_t)(mr.first + j) * Hq + h]);
+        float wsum = 0.f;
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < mr.count; ++j) {
+            const float w = __expf(part_lse[(size_t)(mr.first + j) * Hq + h] - M);
+            const float4 v = *reinterpret_cast<const float4 *>(part_o + ((size_t)(mr.first + j) * Hq + h) * D + c);
+            wsum += w;
+            o.x += w * v.x;
+            o.y += w * v.y;
+            o.z += w * v.z;
+            o.w += w * v.w;
+        }
+        const float inv = 1.f / wsum;
+        __nv_bfloat16 *dst = out + ((size_t)mr.out_token * Hq + h) * D + c;
+        *reinterpret_cast<uint32_t *>(dst) = pack_bf16(o.x * inv, o.y * inv);
+        *reinterpret_cast<uint32_t *>(dst + 2) = pack_bf16(o.z * inv, o.w * inv);
+        if (lse && c == 0) lse[(size_t)mr.out_token * Hq + h] = M + __logf(wsum);
+    }
+}
+
+// Last-page append: one warp per new token copies its K and V rows (num_kv_heads x D
+// bf16 each) to slot rows[t] of the layer slice viewed as [pages * 2 * page_size] rows.
+__global__ void __launch_bounds__(256) append_kernel(const uint4 *k, const uint4 *v, uint4 *cache, const int32_t *rows,
+                                                     int num_tokens, int vec_per_token, int page_size) {
+    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t >= num_tokens) return;
+    const size_t row = (size_t)rows[t];
+    const int lane = threadIdx.x & 31;
+    const uint4 *ks = k + (size_t)t * vec_per_token;
+    const uint4 *vs = v + (size_t)t * vec_per_token;
+    uint4 *kd = cache + row * vec_per_token;
+    uint4 *vd = cache + (row + page_size) * vec_per_token;
+    for (int i = lane; i < vec_per_token; i += 32) {
+        kd[i] = ks[i];
+        vd[i] = vs[i];
+    }
+}
+
+}  // namespace dev
+
+// ------------------------------------------------------------------------------------
+// launchers
+
+static uint32_t decode_stage_bytes(const Shape &s) {
+    return 2u * (uint32_t)s.page_size * s.num_kv_heads * s.head_dim * 2u;
+}
+
+int decode_stages(const Shape &s) {
+    const uint32_t sb = decode_stage_bytes(s);
+    int st = (int)((200u * 1024u) / sb);
+    return st < 2 ? 0 : (st > 8 ? 8 : st);
+}
+
+size_t decode_smem_bytes(const Shape &s) {
+    return 1024 + (size_t)decode_stages(s) * decode_stage_bytes(s) + 2 * 8 * 8;
+}
+
+template <int D, int G>
+static cudaError_t launch_decode_t(const CUtensorMap &tm, const dev::DecodeArgs &a, int grid, int warps, size_t smem,
+                                   cudaStream_t st) {
+    auto fn = dev::decode_kernel<D, G>;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    fn<<<grid, warps * 32, smem, st>>>(tm, a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_decode(const Shape &s, const Plan &p, const CUtensorMap &tm, void *ws, const void *q, void *out,
+                          float *lse, cudaStream_t st) {
+    if (p.dec_ctas == 0) return cudaSuccess;
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    dev::DecodeArgs a;
+    a.q = static_cast<const __nv_bfloat16 *>(q);
+    a.out = static_cast<__nv_bfloat16 *>(out);
+    a.lse = lse;
+    a.tiles = reinterpret_cast<const DecodeTile *>(w + p.lay.dec_tiles);
+    a.cta_ptr = reinterpret_cast<const int32_t *>(w + p.lay.dec_cta_ptr);
+    a.pages = reinterpret_cast<const int32_t *>(w + p.lay.dec_pages);
+    a.part_o = reinterpret_cast<float *>(w + p.lay.part_o);
+    a.part_lse = reinterpret_cast<float *>(w + p.lay.part_lse);
+    a.err = reinterpret_cast<int *>(w + p.lay.err);
+    a.num_qo_heads = s.num_qo_heads;
+    a.num_kv_heads = s.num_kv_heads;
+    a.page_size = s.page_size;
+    a.stages = decode_stages(s);
+    a.stage_bytes = decode_stage_bytes(s);
+    a.box_bytes = (uint32_t)s.page_size * s.num_kv_heads * 128u;
+    a.scale_log2 = p.sm_scale * 1.4426950408889634f;
+    const int warps = s.num_kv_heads + 1;
+    const size_t smem = decode_smem_bytes(s);
+    cudaError_t e = cudaErrorInvalidValue;
+    const int g = s.group();
+#define PKV_DEC(DD, GG) \
+    if (s.head_dim == DD && g == GG) e = launch_decode_t<DD, GG>(tm, a, p.dec_ctas, warps, smem, st);
+    PKV_DEC(64, 1) PKV_DEC(64, 2) PKV_DEC(64, 4) PKV_DEC(64, 8) PKV_DEC(64, 16)
+    PKV_DEC(128, 1) PKV_DEC(128, 2) PKV_DEC(128, 4) PKV_DEC(128, 8) PKV_DEC(128, 16)
+#undef PKV_DEC
+    if (e != cudaSuccess) return e;
+    if (p.num_merge) {
+        dev::merge_kernel<<<p.num_merge, 256, 0, st>>>(reinterpret_cast<const MergeRow *>(w + p.lay.merge_rows),
+                                                        a.part_o, a.part_lse, a.out, lse, s.num_qo_heads,
+                                                        s.head_dim);
+        e = cudaGetLastError();
+    }
+    return e;
+}
+
+cudaError_t launch_append(const Shape &s, const Plan &p, void *ws, const void *k, const void *v, void *kv_layer,
+                          cudaStream_t st) {
+    if (p.num_append == 0) return cudaSuccess;
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    const int vec = s.num_kv_heads * s.head_dim * 2 / 16;
+    const int warps_per_block = 8;
+    const int grid = (p.num_append + warps_per_block - 1) / warps_per_block;
+    dev::append_kernel<<<grid, warps_per_block * 32, 0, st>>>(
+        static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), static_cast<uint4 *>(kv_layer),
+        reinterpret_cast<const int32_t *>(w + p.lay.append_rows), p.num_append, vec, s.page_size);
+    return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -1,0 +1,24 @@
+// Kernel launchers of libpkv (host side), called by the C ABI in pkv_api.cu.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "plan.h"
+
+namespace pkv {
+
+int decode_stages(const Shape &s);
+size_t decode_smem_bytes(const Shape &s);
+size_t prefill_smem_bytes(const Shape &s);
+
+cudaError_t launch_append(const Shape &s, const Plan &p, void *ws, const void *k, const void *v, void *kv_layer,
+                          cudaStream_t st);
+// Decode pass (and the split-KV merge) of a DECODE or MIXED plan; `tm` boxes a whole
+// page of all kv heads.
+cudaError_t launch_decode(const Shape &s, const Plan &p, const CUtensorMap &tm, void *ws, const void *q, void *out,
+                          float *lse, cudaStream_t st);
+// Prefill pass of a PREFILL or MIXED plan; `tm` boxes one page of one kv head.
+cudaError_t launch_prefill(const Shape &s, const Plan &p, const CUtensorMap &tm, void *ws, const void *q, void *out,
+                           float *lse, cudaStream_t st);
+
+}  // namespace pkv

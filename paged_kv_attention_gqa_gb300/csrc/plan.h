@@ -1,0 +1,126 @@
+// Plan structures shared by the host planner and the kernels of libpkv.
+//
+// A plan is made once per step on the host (mstar.engine.resources.attn.wrappers,
+// FlashInfer*Wrapper.plan) and read by every layer's append and run.  Its integer
+// part is built in page-locked host memory and copied into the caller's workspace in
+// one async H2D; the float part (split-KV partials) follows it in the same workspace
+// (mstar.engine.resources.attn.workspace: "the scratch a plan reserves its split-KV
+// partials in").
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <string>
+#include <vector>
+
+namespace pkv {
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
+
+// Query rows of one prefill tile: BQ tokens x all g q-heads of one kv head.
+constexpr int kPrefillRowsPerTile = 128;
+// Keys per prefill K/V stage (4 pages of 16).
+constexpr int kPrefillKeysPerStage = 64;
+
+// One piece of a row's visible pages handled by one decode CTA.
+struct DecodeTile {
+    int32_t q_token;     // token whose query this row uses
+    int32_t out_token;   // token the result is written to, -1 = computed and dropped
+    int32_t kv_base;     // offset of the row's first page in the plan's page list
+    int32_t page_begin;  // first row-local page of this piece
+    int32_t page_count;  // pages in this piece (>= 1)
+    int32_t length;      // L of the row
+    int32_t lo;          // first visible position
+    int32_t partial;     // split-KV partial slot, -1 = this piece is the whole row
+};
+static_assert(sizeof(DecodeTile) == 32, "DecodeTile is 8 ints");
+
+// A row whose visible pages were split over several CTAs: its partials
+// [first, first + count) are merged into out_token.
+struct MergeRow {
+    int32_t out_token;
+    int32_t first;
+    int32_t count;
+    int32_t pad;
+};
+
+// One prefill work tile: up to BQ consecutive new tokens of one row, all q heads of one
+// kv head.
+struct PrefillTile {
+    int32_t q_begin;    // token index (into q / out) of the tile's first query
+    int32_t n_q;        // queries in the tile (1..BQ)
+    int32_t pos0;       // absolute position p of the tile's first query
+    int32_t length;     // L of the row
+    int32_t kv_base;    // offset of the row's first page in the plan's page list
+    int32_t kv_head;    // kv head of the tile
+    int32_t key_begin;  // first key position any query of the tile sees
+    int32_t key_end;    // one past the last key position any query of the tile sees
+};
+static_assert(sizeof(PrefillTile) == 32, "PrefillTile is 8 ints");
+
+// Byte offsets of the plan's arrays inside the workspace.
+struct PlanLayout {
+    size_t err = 0;            // int32 device error word (+ padding)
+    size_t append_rows = 0;    // int32[num_append]: page * 2 * page_size + slot of each new token
+    size_t dec_pages = 0;      // int32[dec_nnz]: page ids the decode pass reads
+    size_t pf_pages = 0;       // int32[pf_nnz]:  page ids the prefill pass reads
+    size_t dec_tiles = 0;      // DecodeTile[dec_tiles]
+    size_t dec_cta_ptr = 0;    // int32[dec_ctas + 1]: tile range of each decode CTA
+    size_t merge_rows = 0;     // MergeRow[num_merge]
+    size_t pf_tiles = 0;       // PrefillTile[pf_tiles]
+    size_t int_bytes = 0;      // end of the integer part (what the H2D copies)
+    size_t part_o = 0;         // float[num_partials, Hq, D]
+    size_t part_lse = 0;       // float[num_partials, Hq]
+    size_t total = 0;          // workspace bytes this plan needs
+};
+
+// Static shape, fixed per handle.
+struct Shape {
+    int num_qo_heads, num_kv_heads, head_dim, page_size;
+    int max_batch, max_total_tokens, max_num_pages, num_cache_pages, max_prefill_rows;
+    int sm_count, sink_page;
+    int group() const { return num_qo_heads / num_kv_heads; }
+};
+
+// Everything a plan produced, host side.  `image` is the integer part exactly as it is
+// copied to the workspace.
+struct Plan {
+    int mode = -1;
+    int batch = 0;
+    int num_tokens = 0;          // T (decode: batch)
+    int causal = 1;
+    int window_left = -1;
+    float sm_scale = 0.f;
+    int num_append = 0;
+    int dec_rows = 0;            // rows of the decode pass (0 when the mode has none)
+    int dec_nnz = 0;
+    int pf_nnz = 0;
+    int dec_ctas = 0, dec_tiles = 0, num_partials = 0, num_merge = 0;
+    int pf_tiles = 0;
+    PlanLayout lay;
+    std::vector<uint8_t> image;
+};
+
+// Host planner entry points (plain C++, no CUDA).  Each returns 0 on success, else a
+// pkv_status code with `err` explaining it.
+int validate_rows(const Shape &s, int mode, const int32_t *qo, const int32_t *kvp, const int32_t *kvi,
+                  const int32_t *lpl, int batch, int window_left, std::string &err);
+int append_slots(int page_size, const int32_t *qo, const int32_t *kvp, const int32_t *kvi, const int32_t *lpl,
+                 int batch, int32_t *pages, int32_t *slots, std::string &err);
+struct MixedLayout {
+    std::vector<int32_t> is_decode, prompt_rows, perm, pf_qo_indptr;
+    std::vector<int32_t> dec_kv_indptr, dec_kv_indices, dec_last_page_len, dec_q_token, dec_out_token;
+};
+int mixed_layout(const int32_t *qo, const int32_t *kvp, const int32_t *kvi, const int32_t *lpl, int batch,
+                 int max_prefill_rows, int sink_page, MixedLayout &out, std::string &err);
+// Split the visible pages of a decode pass into per-CTA tiles.
+void decode_split(const Shape &s, int rows, const int32_t *kvp, const int32_t *lpl, const int32_t *q_token,
+                  const int32_t *out_token, int window_left, std::vector<DecodeTile> &tiles,
+                  std::vector<int32_t> &cta_ptr, std::vector<MergeRow> &merges, int &num_partials);
+int decode_cta_limit(const Shape &s);
+int make_plan(const Shape &s, int mode, const int32_t *qo, const int32_t *kvp, const int32_t *kvi,
+              const int32_t *lpl, int batch, int causal, int window_left, float sm_scale, Plan &plan,
+              std::string &err);
+size_t workspace_bound(const Shape &s, int mode);
+
+}  // namespace pkv

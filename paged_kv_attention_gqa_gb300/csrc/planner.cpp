@@ -1,0 +1,440 @@
+// Host planner of libpkv: validation, KV write locations, the decode split-KV work
+// split, the mixed step's permutation and sink routing, prefill tiles, and the
+// workspace image.  Plain C++: it runs (and is tested) on a machine without a GPU.
+//
+// Passages restated:
+//  * mstar.engine.resources.kv.plan, PagedIndptrs / SequenceView.last_page_len: a row of
+//    kv_indptr[r+1]-kv_indptr[r] pages with its last page filled to last_page_len[r]
+//    holds L = (pages-1)*page_size + last_page_len tokens.
+//  * mstar.engine.resources.attn.wrappers, FlashInferDecodeWrapper.plan: the plan
+//    computes the KV write locations; with the post-append arrays a decode token goes to
+//    the last page at slot last_page_len-1, and in general position p goes to page
+//    kv_indices[kv_indptr[r] + p / page_size], slot p % page_size.
+//  * FlashInferPrefillWrapper.plan: window_left preceding positions are visible, -1 = all.
+//  * FlashInferMixedWrapper: one-token rows are the decode rows; every row goes through
+//    the decode plan (non-decode rows read one token of the sink page, result dropped);
+//    at most max_prefill_rows prompt rows go through the prefill plan, their tokens
+//    moved to the front by a permutation.
+//  * mstar.engine.resources.attn.workspace, Workspace: what a plan needs depends on its
+//    rows, heads and the SM count; the split-KV partials live in the workspace.
+#include "plan.h"
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+
+#include "../../include/pkv.h"
+
+namespace pkv {
+
+static int row_len(const int32_t *kvp, const int32_t *lpl, int r, int P) {
+    int np = kvp[r + 1] - kvp[r];
+    return np <= 0 ? 0 : (np - 1) * P + lpl[r];
+}
+
+int validate_rows(const Shape &s, int mode, const int32_t *qo, const int32_t *kvp, const int32_t *kvi,
+                  const int32_t *lpl, int batch, int window_left, std::string &err) {
+    if (batch < 0 || batch > s.max_batch) {
+        err = "batch " + std::to_string(batch) + " outside [0, max_batch=" + std::to_string(s.max_batch) + "]";
+        return PKV_ERR_INVALID;
+    }
+    if (window_left < -1) {
+        err = "window_left must be -1 (unbounded) or >= 0";
+        return PKV_ERR_INVALID;
+    }
+    if (!kvp || !lpl || (batch > 0 && !kvi && kvp[batch] > 0)) {
+        err = "paged_kv_indptr, paged_kv_indices and paged_kv_last_page_len are required";
+        return PKV_ERR_INVALID;
+    }
+    if (mode != PKV_MODE_DECODE && !qo) {
+        err = "qo_indptr is required for prefill and mixed plans";
+        return PKV_ERR_INVALID;
+    }
+    if (kvp[0] != 0 || (qo && qo[0] != 0)) {
+        err = "indptr arrays must start at 0";
+        return PKV_ERR_INVALID;
+    }
+    for (int r = 0; r < batch; ++r) {
+        if (kvp[r + 1] < kvp[r]) {
+            err = "paged_kv_indptr decreases at row " + std::to_string(r);
+            return PKV_ERR_INVALID;
+        }
+        if (qo && qo[r + 1] < qo[r]) {
+            err = "qo_indptr decreases at row " + std::to_string(r);
+            return PKV_ERR_INVALID;
+        }
+    }
+    if (kvp[batch] > s.max_num_pages) {
+        err = "paged_kv_indices has " + std::to_string(kvp[batch]) + " entries, above max_num_pages=" +
+              std::to_string(s.max_num_pages);
+        return PKV_ERR_INVALID;
+    }
+    int T = qo ? qo[batch] : batch;
+    int tok_cap = mode == PKV_MODE_DECODE ? s.max_batch : s.max_total_tokens;
+    if (T > tok_cap) {
+        err = "step has " + std::to_string(T) + " new tokens, above the handle's maximum " + std::to_string(tok_cap);
+        return PKV_ERR_INVALID;
+    }
+    for (int i = 0; i < kvp[batch]; ++i) {
+        if (kvi[i] < 0 || kvi[i] >= s.num_cache_pages) {
+            err = "page id " + std::to_string(kvi[i]) + " at paged_kv_indices[" + std::to_string(i) +
+                  "] outside [0, num_cache_pages=" + std::to_string(s.num_cache_pages) + ")";
+            return PKV_ERR_INVALID;
+        }
+    }
+    for (int r = 0; r < batch; ++r) {
+        int np = kvp[r + 1] - kvp[r];
+        int n = qo ? qo[r + 1] - qo[r] : 1;
+        if (np > 0 && (lpl[r] < 1 || lpl[r] > s.page_size)) {
+            err = "paged_kv_last_page_len[" + std::to_string(r) + "]=" + std::to_string(lpl[r]) +
+                  " outside [1, page_size]";
+            return PKV_ERR_INVALID;
+        }
+        int L = row_len(kvp, lpl, r, s.page_size);
+        if (mode == PKV_MODE_DECODE && L < 1) {
+            err = "decode row " + std::to_string(r) + " has no tokens";
+            return PKV_ERR_INVALID;
+        }
+        if (n > L) {
+            err = "row " + std::to_string(r) + " has " + std::to_string(n) + " new tokens but length " +
+                  std::to_string(L);
+            return PKV_ERR_INVALID;
+        }
+        if (mode == PKV_MODE_DECODE && n != 1) {
+            err = "decode rows have exactly one new token";
+            return PKV_ERR_INVALID;
+        }
+    }
+    return PKV_OK;
+}
+
+int append_slots(int P, const int32_t *qo, const int32_t *kvp, const int32_t *kvi, const int32_t *lpl, int batch,
+                 int32_t *pages, int32_t *slots, std::string &err) {
+    for (int r = 0; r < batch; ++r) {
+        int L = row_len(kvp, lpl, r, P);
+        int t0 = qo ? qo[r] : r;
+        int n = qo ? qo[r + 1] - qo[r] : 1;
+        if (n > L) {
+            err = "row " + std::to_string(r) + " has more new tokens than its length";
+            return PKV_ERR_INVALID;
+        }
+        for (int i = 0; i < n; ++i) {
+            int p = L - n + i;
+            pages[t0 + i] = kvi[kvp[r] + p / P];
+            slots[t0 + i] = p % P;
+        }
+    }
+    return PKV_OK;
+}
+
+int mixed_layout(const int32_t *qo, const int32_t *kvp, const int32_t *kvi, const int32_t *lpl, int batch,
+                 int max_prefill_rows, int sink_page, MixedLayout &m, std::string &err) {
+    int T = qo[batch];
+    m.is_decode.assign(batch, 0);
+    m.prompt_rows.assign(std::max(max_prefill_rows, 0), -1);
+    m.perm.clear();
+    m.perm.reserve(T);
+    m.pf_qo_indptr.assign(1, 0);
+    int np = 0;
+    for (int r = 0; r < batch; ++r) {
+        int n = qo[r + 1] - qo[r];
+        m.is_decode[r] = n == 1;
+        if (n >= 2) {
+            if (np >= max_prefill_rows) {
+                err = "mixed step has more than max_prefill_rows=" + std::to_string(max_prefill_rows) +
+                      " prompt rows";
+                return PKV_ERR_TOO_MANY_PREFILL_ROWS;
+            }
+            m.prompt_rows[np++] = r;
+            for (int t = qo[r]; t < qo[r + 1]; ++t) m.perm.push_back(t);
+            m.pf_qo_indptr.push_back((int32_t)m.perm.size());
+        }
+    }
+    while ((int)m.pf_qo_indptr.size() < max_prefill_rows + 1) m.pf_qo_indptr.push_back((int32_t)m.perm.size());
+    for (int r = 0; r < batch; ++r)
+        if (qo[r + 1] - qo[r] < 2)
+            for (int t = qo[r]; t < qo[r + 1]; ++t) m.perm.push_back(t);
+    m.dec_kv_indptr.assign(1, 0);
+    m.dec_kv_indices.clear();
+    m.dec_last_page_len.clear();
+    m.dec_q_token.clear();
+    m.dec_out_token.clear();
+    for (int r = 0; r < batch; ++r) {
+        int n = qo[r + 1] - qo[r];
+        if (n == 1) {
+            for (int i = kvp[r]; i < kvp[r + 1]; ++i) m.dec_kv_indices.push_back(kvi[i]);
+            m.dec_last_page_len.push_back(lpl[r]);
+            m.dec_out_token.push_back(qo[r]);
+        } else {
+            if (sink_page < 0) {
+                err = "mixed step with a non-decode row needs a sink_page";
+                return PKV_ERR_INVALID;
+            }
+            m.dec_kv_indices.push_back(sink_page);
+            m.dec_last_page_len.push_back(1);
+            m.dec_out_token.push_back(-1);
+        }
+        m.dec_kv_indptr.push_back((int32_t)m.dec_kv_indices.size());
+        m.dec_q_token.push_back(n >= 1 ? qo[r] : std::max(T - 1, 0));
+    }
+    return PKV_OK;
+}
+
+int decode_cta_limit(const Shape &s) {
+    // One persistent decode CTA per SM: each holds a multi-page ring of whole pages.
+    return std::max(1, s.sm_count);
+}
+
+// Pages each decode CTA is given at least (fewer pages per CTA would only multiply
+// partials without shortening the critical path).
+static constexpr int kMinPagesPerCta = 2;
+
+void decode_split(const Shape &s, int rows, const int32_t *kvp, const int32_t *lpl, const int32_t *q_token,
+                  const int32_t *out_token, int window_left, std::vector<DecodeTile> &tiles,
+                  std::vector<int32_t> &cta_ptr, std::vector<MergeRow> &merges, int &num_partials) {
+    const int P = s.page_size;
+    tiles.clear();
+    cta_ptr.assign(1, 0);
+    merges.clear();
+    num_partials = 0;
+    std::vector<int> first(rows), vis(rows), len(rows), lo(rows);
+    long long W = 0;
+    for (int r = 0; r < rows; ++r) {
+        int L = row_len(kvp, lpl, r, P);
+        int p = L - 1;
+        int l0 = window_left >= 0 ? std::max(0, p - window_left) : 0;
+        len[r] = L;
+        lo[r] = l0;
+        first[r] = l0 / P;
+        vis[r] = (L - 1) / P - first[r] + 1;
+        W += vis[r];
+    }
+    if (W == 0) return;
+    long long cmax = decode_cta_limit(s);
+    long long per = std::max<long long>((W + cmax - 1) / cmax, kMinPagesPerCta);
+    int ctas = (int)((W + per - 1) / per);
+    // Walk the rows' visible pages in order, cutting every `per` pages.
+    std::vector<std::vector<int>> row_tiles(rows);
+    int r = 0, used = 0;  // pages of row r already assigned
+    for (int c = 0; c < ctas; ++c) {
+        long long budget = per;
+        while (budget > 0 && r < rows) {
+            int take = (int)std::min<long long>(budget, vis[r] - used);
+            if (take > 0) {
+                DecodeTile t;
+                t.q_token = q_token[r];
+                t.out_token = out_token[r];
+                t.kv_base = kvp[r];
+                t.page_begin = first[r] + used;
+                t.page_count = take;
+                t.length = len[r];
+                t.lo = lo[r];
+                t.partial = -1;
+                row_tiles[r].push_back((int)tiles.size());
+                tiles.push_back(t);
+                used += take;
+                budget -= take;
+            }
+            if (used == vis[r]) {
+                ++r;
+                used = 0;
+            }
+        }
+        cta_ptr.push_back((int32_t)tiles.size());
+    }
+    for (int rr = 0; rr < rows; ++rr) {
+        if (row_tiles[rr].size() <= 1) continue;
+        MergeRow m;
+        m.out_token = out_token[rr];
+        m.first = num_partials;
+        m.count = (int)row_tiles[rr].size();
+        m.pad = rr;
+        for (int ti : row_tiles[rr]) tiles[ti].partial = num_partials++;
+        merges.push_back(m);
+    }
+}
+
+static void prefill_tiles(const Shape &s, const std::vector<int> &rows, const int32_t *q_begin_of_row,
+                          const int32_t *qo, const int32_t *kvp, const int32_t *lpl, int causal, int window_left,
+                          std::vector<PrefillTile> &out) {
+    const int P = s.page_size;
+    const int g = s.group();
+    const int BQ = kPrefillRowsPerTile / g;
+    for (int r : rows) {
+        int n = qo[r + 1] - qo[r];
+        if (n <= 0) continue;
+        int L = row_len(kvp, lpl, r, P);
+        int c = L - n;
+        for (int t0 = 0; t0 < n; t0 += BQ) {
+            int nq = std::min(BQ, n - t0);
+            int p0 = c + t0, p1 = c + t0 + nq - 1;
+            int kb = window_left >= 0 ? std::max(0, p0 - window_left) : 0;
+            int ke = causal ? p1 + 1 : L;
+            for (int hk = 0; hk < s.num_kv_heads; ++hk) {
+                PrefillTile t;
+                t.q_begin = q_begin_of_row[r] + t0;
+                t.n_q = nq;
+                t.pos0 = p0;
+                t.length = L;
+                t.kv_base = kvp[r];
+                t.kv_head = hk;
+                t.key_begin = kb;
+                t.key_end = ke;
+                out.push_back(t);
+            }
+        }
+    }
+    // Longest first, so the hardware's in-order CTA dispatch approximates LPT.
+    std::stable_sort(out.begin(), out.end(), [](const PrefillTile &a, const PrefillTile &b) {
+        return (a.key_end - a.key_begin) > (b.key_end - b.key_begin);
+    });
+}
+
+static int prefill_tile_bound(const Shape &s, int rows, int tokens) {
+    const int BQ = kPrefillRowsPerTile / s.group();
+    return (tokens / BQ + rows) * s.num_kv_heads;
+}
+
+static PlanLayout layout_for(const Shape &s, int num_append, int dec_nnz, int pf_nnz, int dec_tiles, int dec_ctas,
+                             int num_merge, int pf_tiles, int num_partials) {
+    PlanLayout L;
+    size_t at = 0;
+    L.err = at;
+    at = align_up(at + 16);
+    L.append_rows = at;
+    at = align_up(at + sizeof(int32_t) * (size_t)num_append);
+    L.dec_pages = at;
+    at = align_up(at + sizeof(int32_t) * (size_t)dec_nnz);
+    L.pf_pages = at;
+    at = align_up(at + sizeof(int32_t) * (size_t)pf_nnz);
+    L.dec_tiles = at;
+    at = align_up(at + sizeof(DecodeTile) * (size_t)dec_tiles);
+    L.dec_cta_ptr = at;
+    at = align_up(at + sizeof(int32_t) * (size_t)(dec_ctas + 1));
+    L.merge_rows = at;
+    at = align_up(at + sizeof(MergeRow) * (size_t)num_merge);
+    L.pf_tiles = at;
+    at = align_up(at + sizeof(PrefillTile) * (size_t)pf_tiles);
+    L.int_bytes = at;
+    L.part_o = at;
+    at = align_up(at + sizeof(float) * (size_t)num_partials * s.num_qo_heads * s.head_dim);
+    L.part_lse = at;
+    at = align_up(at + sizeof(float) * (size_t)num_partials * s.num_qo_heads);
+    L.total = at;
+    return L;
+}
+
+size_t workspace_bound(const Shape &s, int mode) {
+    int C = decode_cta_limit(s);
+    int tokens = mode == PKV_MODE_DECODE ? s.max_batch : s.max_total_tokens;
+    int rows = s.max_batch;
+    int dec_rows = mode == PKV_MODE_PREFILL ? 0 : rows;
+    int dec_nnz = mode == PKV_MODE_DECODE ? s.max_num_pages : (mode == PKV_MODE_MIXED ? s.max_num_pages + rows : 0);
+    int pf_nnz = mode == PKV_MODE_DECODE ? 0 : s.max_num_pages;
+    int dec_tiles = dec_rows ? dec_rows + C : 0;
+    int dec_ctas = dec_rows ? C : 0;
+    int num_merge = dec_rows ? C : 0;
+    int pf_rows = mode == PKV_MODE_MIXED ? std::min(rows, s.max_prefill_rows) : rows;
+    int pf_tiles = mode == PKV_MODE_DECODE ? 0 : prefill_tile_bound(s, pf_rows, tokens);
+    int partials = dec_rows ? dec_rows + C : 0;
+    return layout_for(s, tokens, dec_nnz, pf_nnz, dec_tiles, dec_ctas, num_merge, pf_tiles, partials).total;
+}
+
+template <class T>
+static void put(std::vector<uint8_t> &img, size_t off, const T *src, size_t n) {
+    if (n) std::memcpy(img.data() + off, src, n * sizeof(T));
+}
+
+int make_plan(const Shape &s, int mode, const int32_t *qo, const int32_t *kvp, const int32_t *kvi,
+              const int32_t *lpl, int batch, int causal, int window_left, float sm_scale, Plan &plan,
+              std::string &err) {
+    int rc = validate_rows(s, mode, qo, kvp, kvi, lpl, batch, window_left, err);
+    if (rc) return rc;
+    plan = Plan();
+    plan.mode = mode;
+    plan.batch = batch;
+    plan.causal = causal ? 1 : 0;
+    plan.window_left = window_left;
+    plan.sm_scale = sm_scale > 0.f ? sm_scale : 1.0f / std::sqrt((float)s.head_dim);
+    const int T = qo ? qo[batch] : batch;
+    plan.num_tokens = T;
+    plan.num_append = T;
+    const int P = s.page_size;
+
+    std::vector<int32_t> pages(T), slots(T), app(T);
+    rc = append_slots(P, mode == PKV_MODE_DECODE ? nullptr : qo, kvp, kvi, lpl, batch, pages.data(), slots.data(), err);
+    if (rc) return rc;
+    for (int t = 0; t < T; ++t) app[t] = pages[t] * 2 * P + slots[t];
+
+    std::vector<DecodeTile> dtiles;
+    std::vector<int32_t> cta_ptr;
+    std::vector<MergeRow> merges;
+    std::vector<PrefillTile> ptiles;
+    std::vector<int32_t> dec_pages, pf_pages;
+    int partials = 0;
+
+    if (mode == PKV_MODE_DECODE) {
+        std::vector<int32_t> qt(batch), ot(batch);
+        for (int r = 0; r < batch; ++r) qt[r] = ot[r] = r;
+        decode_split(s, batch, kvp, lpl, qt.data(), ot.data(), window_left, dtiles, cta_ptr, merges, partials);
+        dec_pages.assign(kvi, kvi + kvp[batch]);
+        plan.dec_rows = batch;
+    } else if (mode == PKV_MODE_PREFILL) {
+        std::vector<int> rows(batch);
+        for (int r = 0; r < batch; ++r) rows[r] = r;
+        prefill_tiles(s, rows, qo, qo, kvp, lpl, causal, window_left, ptiles);
+        pf_pages.assign(kvi, kvi + kvp[batch]);
+    } else if (mode == PKV_MODE_MIXED) {
+        MixedLayout m;
+        rc = mixed_layout(qo, kvp, kvi, lpl, batch, s.max_prefill_rows, s.sink_page, m, err);
+        if (rc) return rc;
+        if (m.dec_kv_indices.size() > 0 && s.sink_page >= s.num_cache_pages) {
+            err = "sink_page outside the cache";
+            return PKV_ERR_INVALID;
+        }
+        // Decode pass over every row: a decode row attends its own pages, any other row
+        // one token of the sink page; the latter's result is dropped (out_token -1).
+        decode_split(s, batch, m.dec_kv_indptr.data(), m.dec_last_page_len.data(), m.dec_q_token.data(),
+                     m.dec_out_token.data(), window_left, dtiles, cta_ptr, merges, partials);
+        dec_pages = m.dec_kv_indices;
+        plan.dec_rows = batch;
+        // Prefill pass over the prompt rows.  The permutation puts each prompt row's
+        // tokens into one contiguous run of the permuted order; the run of prompt row k
+        // starts at permuted index pf_qo_indptr[k], i.e. at original token
+        // perm[pf_qo_indptr[k]], so the prefill pass reads and writes q / out at those
+        // original offsets directly.
+        std::vector<int> rows;
+        std::vector<int32_t> qbeg(batch, 0);
+        for (int k = 0; k < s.max_prefill_rows; ++k) {
+            int r = m.prompt_rows[k];
+            if (r < 0) continue;
+            rows.push_back(r);
+            qbeg[r] = m.perm[m.pf_qo_indptr[k]];
+        }
+        prefill_tiles(s, rows, qbeg.data(), qo, kvp, lpl, causal, window_left, ptiles);
+        pf_pages.assign(kvi, kvi + kvp[batch]);
+    } else {
+        err = "unknown plan mode";
+        return PKV_ERR_INVALID;
+    }
+    plan.dec_nnz = (int)dec_pages.size();
+    plan.pf_nnz = (int)pf_pages.size();
+    plan.dec_tiles = (int)dtiles.size();
+    plan.dec_ctas = dtiles.empty() ? 0 : (int)cta_ptr.size() - 1;
+    plan.num_merge = (int)merges.size();
+    plan.num_partials = partials;
+    plan.pf_tiles = (int)ptiles.size();
+    plan.lay = layout_for(s, T, plan.dec_nnz, plan.pf_nnz, plan.dec_tiles, plan.dec_ctas, plan.num_merge,
+                          plan.pf_tiles, partials);
+    plan.image.assign(plan.lay.int_bytes, 0);
+    put(plan.image, plan.lay.append_rows, app.data(), app.size());
+    put(plan.image, plan.lay.dec_pages, dec_pages.data(), dec_pages.size());
+    put(plan.image, plan.lay.pf_pages, pf_pages.data(), pf_pages.size());
+    put(plan.image, plan.lay.dec_tiles, dtiles.data(), dtiles.size());
+    if (plan.dec_ctas) put(plan.image, plan.lay.dec_cta_ptr, cta_ptr.data(), cta_ptr.size());
+    put(plan.image, plan.lay.merge_rows, merges.data(), merges.size());
+    put(plan.image, plan.lay.pf_tiles, ptiles.data(), ptiles.size());
+    return PKV_OK;
+}
+
+}  // namespace pkv

@@ -1,0 +1,209 @@
+"""CUDA path (through the C ABI) against the oracle on the same seeded inputs.
+
+Index and addressing work is compared bit-exactly (the appended cache, every byte of
+the layer slice); attention outputs at max-abs 2e-2, relative L2 1e-2, lse 1e-3
+relative (|d| <= 1e-3 max(1, |lse|)).  Free pages and page tails hold bf16 NaN unless a
+case says otherwise, so any read past a row's end shows up.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import gpu_util as G
+from paged_kv_attention_gqa_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover - collected on CPU, skipped there
+    pytest.skip("needs a GPU", allow_module_level=True)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _build():
+    from paged_kv_attention_gqa_gb300 import build
+    build.build()
+
+
+def _check_step(pb, mode, *, window_left=-1, causal=True, sm_scale=0.0, sm_count=0, seed=0, unused="nan",
+                rows=None):
+    x = wl.make_inputs(pb, device="cuda", seed=seed, unused=unused, layers=1)
+    before = wl.bf16_bits(x["kv_cache"][0])
+    out, lse, h, ws = G.gpu_step(pb, x, mode, window_left=window_left, causal=causal, sm_scale=sm_scale,
+                                 sm_count=sm_count)
+    after = G.oracle_append(pb, before, x)
+    got = wl.bf16_bits(x["kv_cache"][0])
+    assert np.array_equal(got, after), "appended cache differs from the oracle's (bit-exact)"
+    ref_o, ref_l = G.oracle_attn(pb, wl.bf16_bits(x["q"]), after, causal=causal if mode != "decode" else True,
+                                 window_left=window_left, sm_scale=sm_scale, rows=rows)
+    tokens = None if rows is None else G.token_mask(pb, rows)
+    return G.compare(out, lse, ref_o, ref_l, tokens=tokens, what=f"{pb.name}/{mode}")
+
+
+# ------------------------------------------------------------------ decode
+
+def test_tiny_decode_config():
+    pb = wl.config_tiny()
+    _check_step(pb, "decode")
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (8, 4), (8, 2), (16, 2), (32, 2)])
+def test_decode_groups_and_dims(D, Hq, Hkv):
+    lens = [1, 2, 15, 16, 17, 31, 32, 33, 100, 257, 1000]
+    pb = wl.custom(3, lens, [1] * len(lens), num_qo_heads=Hq, num_kv_heads=Hkv, head_dim=D, page_size=16,
+                   pool_factor=1.3)
+    _check_step(pb, "decode", seed=1)
+
+
+@pytest.mark.parametrize("window", [0, 1, 5, 15, 16, 17, 100])
+def test_decode_window(window):
+    lens = [1, 5, 16, 17, 40, 300, 1500]
+    pb = wl.custom(4, lens, [1] * len(lens), num_qo_heads=32, num_kv_heads=8, head_dim=128, page_size=16)
+    _check_step(pb, "decode", window_left=window, seed=2)
+
+
+@pytest.mark.parametrize("sm_count", [1, 2, 3, 7, 152, 300])
+def test_decode_forced_splits(sm_count):
+    lens = [700, 33, 1, 2048, 129, 16, 4000]
+    pb = wl.custom(5, lens, [1] * len(lens), num_qo_heads=64, num_kv_heads=8, head_dim=128, page_size=16)
+    _check_step(pb, "decode", sm_count=sm_count, seed=3)
+
+
+def test_decode_sm_scale():
+    pb = wl.custom(6, [90, 400], [1, 1], num_qo_heads=32, num_kv_heads=8, head_dim=128, page_size=16)
+    _check_step(pb, "decode", sm_scale=0.3, seed=4)
+
+
+def test_decode_page_pool_permutation_is_bit_identical():
+    import oracle_pins
+    pb = wl.custom(7, [300, 17, 1000, 64], [1, 1, 1, 1], num_qo_heads=32, num_kv_heads=8, head_dim=128,
+                   page_size=16, pool_factor=1.5)
+    x = wl.make_inputs(pb, device="cuda", seed=5, unused="nan", layers=1)
+    out1, lse1, _, _ = G.gpu_step(pb, x, "decode")
+    pb2, kv2 = oracle_pins.relabel_pool(pb, x["kv_cache"][0], seed=9)
+    x2 = dict(x, kv_cache=kv2.unsqueeze(0))
+    out2, lse2, _, _ = G.gpu_step(pb2, x2, "decode", append=False)
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(lse1, lse2)
+
+
+def test_empty_batch_is_a_no_op():
+    pb = wl.custom(8, [5], [1], num_qo_heads=8, num_kv_heads=2, head_dim=64, page_size=16)
+    h = G.make_handle(pb)
+    ws = torch.empty(h.workspace_size(0), dtype=torch.uint8, device="cuda")
+    h.plan(0, None, [0], [], [], workspace=ws)
+    q = torch.zeros(0, 8, 64, dtype=torch.bfloat16, device="cuda")
+    kv = torch.zeros(pb.max_pages, 2, 16, 2, 64, dtype=torch.bfloat16, device="cuda")
+    h.run_decode(q, kv, q, None, workspace=ws)
+    torch.cuda.synchronize()
+
+
+# ------------------------------------------------------------------ prefill
+
+@pytest.mark.parametrize("D,Hq,Hkv", [(128, 32, 8), (64, 8, 8), (128, 16, 2), (64, 32, 2)])
+@pytest.mark.parametrize("causal", [True, False])
+def test_prefill_ragged(D, Hq, Hkv, causal):
+    n = [1, 7, 33, 130, 64, 2]
+    c = [0, 40, 0, 300, 17, 1]
+    pb = wl.custom(10, np.add(n, c), n, num_qo_heads=Hq, num_kv_heads=Hkv, head_dim=D, page_size=16)
+    _check_step(pb, "prefill", causal=causal, seed=6)
+
+
+@pytest.mark.parametrize("window", [0, 3, 16, 63, 64, 200])
+def test_prefill_window(window):
+    n = [200, 5, 70]
+    c = [0, 500, 90]
+    pb = wl.custom(11, np.add(n, c), n, num_qo_heads=32, num_kv_heads=8, head_dim=128, page_size=16)
+    _check_step(pb, "prefill", window_left=window, seed=7)
+
+
+def test_prefill_rows_without_tokens():
+    n = [0, 20, 0, 3]
+    c = [50, 10, 1, 0]
+    pb = wl.custom(12, np.add(n, c), n, num_qo_heads=32, num_kv_heads=8, head_dim=128, page_size=16)
+    _check_step(pb, "prefill", seed=8)
+
+
+# ------------------------------------------------------------------ mixed
+
+def _mixed_batch(seed, n, c, **kw):
+    pb = wl.custom(seed, np.add(n, c), n, num_qo_heads=32, num_kv_heads=8, head_dim=128, page_size=16,
+                   reserve_sink=True, **kw)
+    pb.max_prefill_rows = int((np.asarray(n) >= 2).sum()) + 1
+    return pb
+
+
+def test_mixed_small():
+    n = [1, 1, 40, 1, 3, 1, 0, 1, 100]
+    c = [20, 300, 10, 1, 0, 16, 5, 700, 33]
+    pb = _mixed_batch(13, n, c)
+    _check_step(pb, "mixed", seed=9)
+
+
+def test_mixed_matches_separate_passes():
+    n = [1, 70, 1, 1, 9]
+    c = [33, 0, 500, 1, 60]
+    pb = _mixed_batch(14, n, c)
+    x = wl.make_inputs(pb, device="cuda", seed=10, unused="nan", layers=1)
+    out_m, lse_m, _, _ = G.gpu_step(pb, x, "mixed")
+    # the same rows through the plain prefill plan (no append: the cache already holds them)
+    out_p, lse_p, _, _ = G.gpu_step(pb, x, "prefill", append=False)
+    G.compare(out_m, lse_m, out_p.float().cpu().numpy(), lse_p.cpu().numpy(), what="mixed vs prefill")
+
+
+def test_mixed_poisoned_sink_rows_do_not_leak():
+    """Every prompt row's decode-pass result is dropped: poisoning q of prompt tokens'
+    decode-pass reads cannot reach out (the sink page holds finite values)."""
+    n = [1, 12, 1]
+    c = [5, 3, 40]
+    pb = _mixed_batch(15, n, c)
+    _check_step(pb, "mixed", seed=11)
+
+
+# ------------------------------------------------------------------ full-size configs (launch config of bench.py)
+
+def test_batch_decode_full_size():
+    pb = wl.config_batch_decode()
+    x = wl.make_inputs(pb, device="cuda", seed=0, unused="randn")
+    h = G.make_handle(pb)
+    ws = torch.empty(h.workspace_size(0), dtype=torch.uint8, device="cuda")
+    h.plan(0, None, pb.kv_indptr, pb.kv_indices, pb.last_page_len, workspace=ws)
+    check_layers = {0: None, 31: None, 13: [3, 77, 127]}
+    befores = {l: wl.bf16_bits(x["kv_cache"][l]) for l in check_layers}
+    outs = {}
+    for l in range(pb.num_layers):
+        kv = x["kv_cache"][l]
+        h.kv_append(x["k_new"], x["v_new"], kv, workspace=ws)
+        out = torch.empty_like(x["q"])
+        lse = torch.empty(pb.batch, pb.num_qo_heads, dtype=torch.float32, device="cuda")
+        h.run_decode(x["q"], kv, out, lse, workspace=ws)
+        if l in check_layers:
+            outs[l] = (out, lse)
+    torch.cuda.synchronize()
+    assert h.check_device_error(ws) == 0
+    for l, rows in check_layers.items():
+        after = G.oracle_append(pb, befores[l], x)
+        assert np.array_equal(wl.bf16_bits(x["kv_cache"][l]), after), l
+        ref_o, ref_l = G.oracle_attn(pb, wl.bf16_bits(x["q"]), after, rows=rows, threads=16)
+        G.compare(*outs[l], ref_o, ref_l, tokens=None if rows is None else G.token_mask(pb, rows), what=f"layer {l}")
+
+
+def test_ragged_prefill_full_size():
+    pb = wl.config_prefill()
+    # rows the oracle finishes in seconds: row 0 (prefix 0) and the cheapest others
+    cost = pb.qo_lens * (pb.kv_lens - pb.qo_lens + pb.qo_lens / 2)
+    rows = sorted(set([0] + list(np.argsort(cost)[:3])))
+    _check_step(pb, "prefill", unused="randn", rows=rows)
+
+
+def test_mixed_full_size():
+    pb = wl.config_mixed()
+    _check_step(pb, "mixed", unused="nan")
+
+
+@pytest.mark.parametrize("window", [-1, 4096])
+def test_long_decode_full_size(window):
+    pb = wl.config_long(window_left=window)
+    _check_step(pb, "decode", window_left=window, unused="randn")
