@@ -183,6 +183,30 @@ pkv_status pkv_run_mixed(pkv_handle_t h, const void *q, const void *kv_layer, vo
  */
 pkv_status pkv_check_device_error(pkv_handle_t h, void *workspace, pkv_stream_t stream, int *code);
 
+/*
+ * Decode that needs no workspace: plan + pkv_run_decode in one call, with the plan and
+ * the split-KV partials kept in a 16 MiB scratch array compiled into the library
+ * (one per GPU that loads it, held until the process exits).  The pages have no
+ * counterpart to this call; it exists for callers that are handed only their inputs,
+ * outputs and a stream and may not allocate device memory themselves, e.g. code running
+ * while a CUDA graph is being captured, plugin hooks of inference runtimes, or latency-
+ * critical paths that must not enter an allocator that can synchronise or fail.
+ *   q, out, lse, kv_layer: as pkv_run_decode.  kv_indptr, kv_indices, last_page_len:
+ *   HOST int32 arrays as in pkv_plan (decode: one new token per row).
+ * The call plans on the host (ordinary heap memory only), copies the plan from pageable
+ * memory into the scratch on `stream` (so it may wait for work already queued there), and
+ * launches the decode and merge kernels; it makes no device or page-locked allocation.  Its first call on a device resolves the
+ * scratch's device address (once per device, with that device current): make that first
+ * call before any stream capture.  A decode whose plan needs more than 16 MiB returns
+ * PKV_ERR_WORKSPACE.  Every call shares the one array and overwrites it: calls that
+ * overlap on the GPU (other streams or threads) race; calls on one stream do not.
+ * Device-side wait errors are recorded in the scratch and are not reported.
+ */
+pkv_status pkv_run_decode_static(pkv_handle_t h, const void *q, const void *kv_layer, void *out, float *lse,
+                                 const int32_t *paged_kv_indptr, const int32_t *paged_kv_indices,
+                                 const int32_t *paged_kv_last_page_len, int batch, int window_left, float sm_scale,
+                                 pkv_stream_t stream);
+
 /* ---- host-only planning queries (no CUDA call; usable on a machine without a GPU) ---- */
 
 /*

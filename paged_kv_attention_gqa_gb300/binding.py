@@ -22,7 +22,7 @@ STATUS_NAMES = ["OK", "INVALID", "UNSUPPORTED", "WORKSPACE", "TOO_MANY_PREFILL_R
 # every symbol include/pkv.h declares
 EXPORTS = ["pkv_create", "pkv_destroy", "pkv_last_error", "pkv_workspace_size", "pkv_plan", "pkv_kv_append",
            "pkv_run_decode", "pkv_run_prefill", "pkv_run_mixed", "pkv_check_device_error", "pkv_append_slots",
-           "pkv_mixed_layout", "pkv_decode_split"]
+           "pkv_mixed_layout", "pkv_decode_split", "pkv_run_decode_static"]
 
 
 class PkvError(RuntimeError):
@@ -64,6 +64,7 @@ def load(path: str = LIB_PATH):
         "pkv_append_slots": ([i, i32p, i32p, i32p, i32p, i, i32p, i32p], i),
         "pkv_mixed_layout": ([i32p, i32p, i32p, i32p, i, i, i] + [i32p] * 9 + [ctypes.POINTER(i)], i),
         "pkv_decode_split": ([vp, i32p, i32p, i, i, i32p, ctypes.POINTER(i), ctypes.POINTER(i)], i),
+        "pkv_run_decode_static": ([vp, vp, vp, vp, vp, i32p, i32p, i32p, i, i, ctypes.c_float, vp], i),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)

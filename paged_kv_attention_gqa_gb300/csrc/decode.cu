@@ -22,6 +22,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "launch.h"
 #include "plan.h"
 #include "ptx.cuh"
@@ -416,6 +418,43 @@ cudaError_t launch_append(const Shape &s, const Plan &p, void *ws, const void *k
         static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), static_cast<uint4 *>(kv_layer),
         reinterpret_cast<const int32_t *>(w + p.lay.append_rows), p.num_append, vec, s.page_size);
     return cudaGetLastError();
+}
+
+}  // namespace pkv
+
+// ------------------------------------------------------------------------------------
+// Scratch for callers that cannot allocate device memory (pkv_run_decode_static).
+//
+// The plan image and the split-KV partials of such a call live in this file-scope
+// array instead of a caller workspace.  Every GPU that loads the library holds it until
+// the process exits.  Host code must not use the array's name as an address: its
+// device address is fetched once per device with cudaGetSymbolAddress.
+namespace pkv {
+
+constexpr size_t kStaticScratchBytes = size_t(16) << 20;  // 16 MiB
+
+static __device__ __align__(256) uint8_t g_decode_scratch[kStaticScratchBytes];
+
+size_t static_scratch_bytes() { return kStaticScratchBytes; }
+
+// Device address of g_decode_scratch on the current device.  The first call on a device
+// resolves it (with that device current) and caches it; later calls only read the cache.
+cudaError_t static_scratch(void **ptr) {
+    static std::mutex mu;
+    static void *cached[128] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cached[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_decode_scratch);
+        if (e != cudaSuccess) return e;
+        cached[dev] = p;
+    }
+    *ptr = cached[dev];
+    return cudaSuccess;
 }
 
 }  // namespace pkv

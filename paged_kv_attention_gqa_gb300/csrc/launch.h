@@ -21,4 +21,8 @@ cudaError_t launch_decode(const Shape &s, const Plan &p, const CUtensorMap &tm, 
 cudaError_t launch_prefill(const Shape &s, const Plan &p, const CUtensorMap &tm, void *ws, const void *q, void *out,
                            float *lse, cudaStream_t st);
 
+// File-scope device scratch used by pkv_run_decode_static (see decode.cu).
+size_t static_scratch_bytes();
+cudaError_t static_scratch(void **ptr);
+
 }  // namespace pkv

@@ -355,3 +355,36 @@ extern "C" pkv_status pkv_decode_split(pkv_handle_t h, const int32_t *kvp, const
     *num_ctas = dt.empty() ? 0 : (int)cta.size() - 1;
     return PKV_OK;
 }
+
+// ---------------- decode without a caller workspace ----------------
+
+extern "C" pkv_status pkv_run_decode_static(pkv_handle_t h, const void *q, const void *kv_layer, void *out,
+                                            float *lse, const int32_t *kv_indptr, const int32_t *kv_indices,
+                                            const int32_t *last_page_len, int batch, int window_left, float sm_scale,
+                                            pkv_stream_t stream) {
+    if (!h) return fail(h, PKV_ERR_INVALID, "null handle");
+    if (!(sm_scale >= 0.f) || std::isinf(sm_scale)) return fail(h, PKV_ERR_INVALID, "sm_scale must be finite and >= 0");
+    std::string err;
+    Plan plan;
+    int rc = pkv::make_plan(h->shape, PKV_MODE_DECODE, nullptr, kv_indptr, kv_indices, last_page_len, batch, 1,
+                            window_left, sm_scale, plan, err);
+    if (rc) return fail(h, (pkv_status)rc, err);
+    if (plan.lay.total > pkv::static_scratch_bytes())
+        return fail(h, PKV_ERR_WORKSPACE,
+                    "this decode needs " + std::to_string(plan.lay.total) + " bytes of scratch, above the " +
+                        std::to_string(pkv::static_scratch_bytes()) +
+                        "-byte static scratch of pkv_run_decode_static; use pkv_plan + pkv_run_decode with a workspace");
+    if (batch == 0) return PKV_OK;
+    pkv_status st = check_io(h, q, kv_layer, out);
+    if (st != PKV_OK) return st;
+    void *scratch = nullptr;
+    cudaError_t e = pkv::static_scratch(&scratch);
+    if (e != cudaSuccess) return cuda_fail(h, e, "static scratch address");
+    if ((st = dec_map(h, kv_layer)) != PKV_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // The plan image (its error word zeroed) overwrites the previous call's contents.
+    e = cudaMemcpyAsync(scratch, plan.image.data(), plan.image.size(), cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "static plan H2D");
+    e = pkv::launch_decode(h->shape, plan, h->tm_dec, scratch, q, out, lse, s);
+    return e == cudaSuccess ? PKV_OK : cuda_fail(h, e, "static decode launch");
+}
