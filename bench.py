@@ -97,7 +97,7 @@ class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled every 100 ms during the timed region."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,clocks.mem")
 
     def __init__(self):
         self.proc = None
@@ -130,19 +130,19 @@ class ClockSampler:
         rows = []
         for line in open(self.path):
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9], float(parts[9])))
             except ValueError:
                 continue
         os.unlink(self.path)
         if not rows:
             return None
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower().startswith("active")})
+        reasons = sorted({names[i] for _, _, r, _ in rows for i, v in enumerate(r) if v.lower().startswith("active")})
         return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
-                "reasons": reasons, "samples": len(rows)}
+                "mem_mhz": statistics.median(r[3] for r in rows), "reasons": reasons, "samples": len(rows)}
 
 
 def kernel_traffic(kernel_file: str, summary: str):

@@ -14,7 +14,7 @@ ROOT = os.path.dirname(PKG)
 OUT = os.path.join(PKG, "libpkv.so")
 OBJ = os.path.join(PKG, "_build")
 SOURCES = ["pkv_api.cu", "decode.cu", "prefill.cu", "planner.cpp"]
-HEADERS = ["plan.h", "launch.h", "ptx.cuh"]
+HEADERS = ["plan.h", "launch.h", "ptx.cuh", "tcgen05.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -17,9 +17,10 @@ cudaError_t launch_append(const Shape &s, const Plan &p, void *ws, const void *k
 // page of all kv heads.
 cudaError_t launch_decode(const Shape &s, const Plan &p, const CUtensorMap &tm, void *ws, const void *q, void *out,
                           float *lse, cudaStream_t st);
-// Prefill pass of a PREFILL or MIXED plan; `tm` boxes one page of one kv head.
-cudaError_t launch_prefill(const Shape &s, const Plan &p, const CUtensorMap &tm, void *ws, const void *q, void *out,
-                           float *lse, cudaStream_t st);
+// Prefill pass of a PREFILL or MIXED plan; `tm_kv` boxes one page of one kv head, `tm_q`
+// boxes (64 columns, g heads, 128/g tokens) of q viewed as [tokens][Hq][D].
+cudaError_t launch_prefill(const Shape &s, const Plan &p, const CUtensorMap &tm_kv, const CUtensorMap &tm_q, void *ws,
+                           void *out, float *lse, cudaStream_t st);
 
 // File-scope device scratch used by pkv_run_decode_static (see decode.cu).
 size_t static_scratch_bytes();

@@ -29,8 +29,9 @@ struct pkv_handle_s {
     bool fence_live[2] = {false, false};
     int ring_at = 0;
     // last encoded tensor maps (re-encoded when the layer pointer changes)
-    const void *tm_dec_ptr = nullptr, *tm_pf_ptr = nullptr;
-    CUtensorMap tm_dec{}, tm_pf{};
+    const void *tm_dec_ptr = nullptr, *tm_pf_ptr = nullptr, *tm_q_ptr = nullptr;
+    int tm_q_rows = -1;
+    CUtensorMap tm_dec{}, tm_pf{}, tm_q{};
 };
 
 static thread_local std::string g_create_err;
@@ -194,6 +195,27 @@ static pkv_status encode_kv(pkv_handle_t h, const void *kv_layer, int box_heads,
     return PKV_OK;
 }
 
+// Tensor map over q viewed as [tokens][Hq][D]: a box of (64 columns, g heads, 128 / g
+// tokens) lands as 128 query rows (token-major, head-minor) of 128 bytes, 128-byte swizzled.
+static pkv_status q_map(pkv_handle_t h, const void *q, int rows) {
+    if (h->tm_q_ptr == q && h->tm_q_rows == rows) return PKV_OK;
+    auto fn = encode_fn();
+    if (!fn) return fail(h, PKV_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+    const Shape &s = h->shape;
+    const int g = s.group();
+    cuuint64_t dims[3] = {(cuuint64_t)s.head_dim, (cuuint64_t)s.num_qo_heads, (cuuint64_t)rows};
+    cuuint64_t strides[2] = {(cuuint64_t)s.head_dim * 2, (cuuint64_t)s.num_qo_heads * s.head_dim * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)g, (cuuint32_t)(pkv::kPrefillRowsPerTile / g)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(&h->tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(h, PKV_ERR_CUDA, "cuTensorMapEncodeTiled (q) failed (" + std::to_string((int)r) + ")");
+    h->tm_q_ptr = q;
+    h->tm_q_rows = rows;
+    return PKV_OK;
+}
+
 static pkv_status check_planned(pkv_handle_t h, void *ws, int mode_a, int mode_b = -1) {
     if (!h) return PKV_ERR_INVALID;
     if (!h->planned_ws || h->planned_ws != ws)
@@ -255,7 +277,8 @@ extern "C" pkv_status pkv_run_prefill(pkv_handle_t h, const void *q, const void 
     if (h->plan.num_tokens == 0) return PKV_OK;
     if ((st = check_io(h, q, kv_layer, out)) != PKV_OK) return st;
     if ((st = pf_map(h, kv_layer)) != PKV_OK) return st;
-    cudaError_t e = pkv::launch_prefill(h->shape, h->plan, h->tm_pf, workspace, q, out, lse,
+    if ((st = q_map(h, q, h->plan.num_tokens)) != PKV_OK) return st;
+    cudaError_t e = pkv::launch_prefill(h->shape, h->plan, h->tm_pf, h->tm_q, workspace, out, lse,
                                         static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PKV_OK : cuda_fail(h, e, "prefill launch");
 }
@@ -268,10 +291,11 @@ extern "C" pkv_status pkv_run_mixed(pkv_handle_t h, const void *q, const void *k
     if ((st = check_io(h, q, kv_layer, out)) != PKV_OK) return st;
     if ((st = dec_map(h, kv_layer)) != PKV_OK) return st;
     if ((st = pf_map(h, kv_layer)) != PKV_OK) return st;
+    if ((st = q_map(h, q, h->plan.num_tokens)) != PKV_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = pkv::launch_decode(h->shape, h->plan, h->tm_dec, workspace, q, out, lse, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "mixed decode-pass launch");
-    e = pkv::launch_prefill(h->shape, h->plan, h->tm_pf, workspace, q, out, lse, s);
+    e = pkv::launch_prefill(h->shape, h->plan, h->tm_pf, h->tm_q, workspace, out, lse, s);
     return e == cudaSuccess ? PKV_OK : cuda_fail(h, e, "mixed prefill-pass launch");
 }
 

@@ -1,17 +1,26 @@
 // Ragged paged prefill over a cached prefix (FlashInferPrefillWrapper.run), also the
 // prefill pass of the mixed step (FlashInferMixedWrapper).
 //
-// New token i of row r sits at position p = L_r - n_r + i and sees keys
-// [lo, p] (causal, bottom-right aligned: "the cached prefix plus themselves") or
-// [lo, L_r - 1] (non-causal), lo = max(0, p - window_left) or 0.
+// New token i of row r sits at position p = L_r - n_r + i and sees keys [lo, p] (causal,
+// bottom-right aligned: "the cached prefix plus themselves") or [lo, L_r - 1]
+// (non-causal), lo = max(0, p - window_left) or 0.
 //
-// A CTA takes one tile: up to BQ = 128 / g consecutive new tokens of one row and all g
-// query heads of one kv head, i.e. 128 query rows sharing every K/V tile.  A producer
-// thread streams 64-key stages (4 pages of that kv head, K and V, 64-column halves with
-// 128-byte swizzle) by TMA; a page past the row's end is fetched at an out-of-range
-// coordinate, which TMA fills with zeros.  Eight consumer warps own 16 query rows each
-// and run QK^T and PV as 16x8x16 bf16 tensor-core MMAs with an exp2-domain online
-// softmax.
+// A CTA computes one tile: up to BQ = 128 / g consecutive new tokens of one row times
+// the g query heads of one kv head = 128 query rows (row m = token * g + head), which
+// share every K/V tile.  Blackwell design, two CTAs per SM:
+//  * warp 4 (one thread) loads Q once and streams 64-key K and V tiles (four 16-slot
+//    pages of the kv head, 64-column halves, 128-byte swizzle) by TMA into a two-stage
+//    ring; a page past the row's end is fetched at an out-of-range coordinate, which TMA
+//    fills with zeros;
+//  * warp 5 owns 256 tensor-memory columns: S double-buffered (2 x 64 fp32 columns) and
+//    O (D fp32 columns); one thread issues S_j = Q K_j^T (tcgen05.mma, both operands in
+//    shared memory, K-major) and then O += P_{j-1} V_{j-1} (P read from tensor memory,
+//    V from shared memory MN-major), committing each group to mbarriers;
+//  * warps 0-3 (thread = query row = TMEM lane) read S, mask, run the online softmax in
+//    the exp2 domain and write P as packed bf16 over the S columns they just read.  The
+//    running maximum is only moved (and O rescaled in tensor memory) when it grows by
+//    more than 2^8, so most tiles never touch O;
+//  * the epilogue reads O, divides by the row sum and stores bf16 rows and the lse.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -19,12 +28,12 @@
 #include "launch.h"
 #include "plan.h"
 #include "ptx.cuh"
+#include "tcgen05.cuh"
 
 namespace pkv {
 namespace dev {
 
 struct PrefillArgs {
-    const __nv_bfloat16 *q;
     __nv_bfloat16 *out;
     float *lse;
     const PrefillTile *tiles;
@@ -32,267 +41,340 @@ struct PrefillArgs {
     int *err;
     int num_qo_heads;
     int page_size;
-    int oob_row;       // a row coordinate past the cache: TMA fills it with zeros
-    int stages;
-    uint32_t stage_bytes;
+    int oob_row;  // a row coordinate past the cache: TMA fills it with zeros
     int causal;
     int window_left;
     float scale_log2;
 };
 
-constexpr int kConsumerWarps = 8;
+constexpr int kPfThreads = 192;  // warps 0-3 softmax, 4 producer, 5 MMA
+constexpr int kPfKeys = kPrefillKeysPerStage;  // 64 keys per K/V tile
+constexpr int kPfStages = 2;
+constexpr uint32_t kPfTmemCols = 256;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kLn2f = 0.6931471805599453f;
 
-template <int D, int G>
-__global__ void __launch_bounds__((kConsumerWarps + 1) * 32, 1)
-    prefill_kernel(const __grid_constant__ CUtensorMap tmap, const PrefillArgs a) {
-    constexpr int HALVES = D / 64;
-    constexpr int KEYS = kPrefillKeysPerStage;       // 64 keys per stage
-    constexpr int BOX = 16 * 128;                    // one page (16 slots) x 64 columns
-    constexpr int BLOCK = KEYS * 128;                // one (K|V, half) block of a stage
-    constexpr int BQ = kPrefillRowsPerTile / G;      // query tokens per tile
-    constexpr int KS = D / 16;
-    constexpr int NT = D / 8;
-    static_assert(KEYS == 4 * 16, "a stage is four 16-slot pages");
+template <int D>
+struct PfSmem {
+    static constexpr int HALVES = D / 64;
+    static constexpr uint32_t Q_BYTES = 128u * D * 2;
+    static constexpr uint32_t KV_BYTES = (uint32_t)kPfKeys * D * 2;  // one K or V tile
+    static constexpr uint32_t Q_OFF = 0;
+    static constexpr uint32_t K_OFF = Q_BYTES;
+    static constexpr uint32_t V_OFF = K_OFF + kPfStages * KV_BYTES;
+    static constexpr uint32_t BAR_OFF = V_OFF + kPfStages * KV_BYTES;
+    static constexpr uint32_t BYTES = BAR_OFF + 256;
+};
 
+template <int D, int G>
+__global__ void __launch_bounds__(kPfThreads, 2)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_q,
+                      const PrefillArgs a) {
+    using L = PfSmem<D>;
+    constexpr int HALVES = L::HALVES;
+    constexpr int BQ = kPrefillRowsPerTile / G;
+    constexpr int KSTEPS = D / 16;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)a.stages * a.stage_bytes);
-    uint64_t *empty = full + a.stages;
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::BAR_OFF);
+    uint64_t *q_full = bars + 0;
+    uint64_t *k_full = bars + 1;   // [2]
+    uint64_t *v_full = bars + 3;   // [2]
+    uint64_t *k_empty = bars + 5;  // [2]
+    uint64_t *v_empty = bars + 7;  // [2]
+    uint64_t *s_full = bars + 9;   // [2]
+    uint64_t *p_full = bars + 11;  // [2]
+    uint64_t *o_done = bars + 13;
+    uint64_t *pv_done = bars + 14;  // [2]: PV_i, which reads P_i from S buffer i & 1, has completed
+    // o_final completes once, after the last PV.  The epilogue cannot wait on o_done by
+    // parity: when it gets there, two PVs may still be outstanding, and phase nt-1 has
+    // the same parity as the already completed phase nt-3.
+    uint64_t *o_final = bars + 16;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 17);
 
     const PrefillTile t = a.tiles[blockIdx.x];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int P = a.page_size;
-    const int kt0 = t.key_begin / KEYS;
-    const int kt1 = (t.key_end + KEYS - 1) / KEYS;
+    const int kt0 = t.key_begin / kPfKeys;
+    const int nt = (t.key_end + kPfKeys - 1) / kPfKeys - kt0;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < a.stages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kConsumerWarps);
+        mbar_init(q_full, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&k_full[s], 1);
+            mbar_init(&v_full[s], 1);
+            mbar_init(&k_empty[s], 1);
+            mbar_init(&v_empty[s], 1);
+            mbar_init(&s_full[s], 1);
+            mbar_init(&p_full[s], 4);
+            mbar_init(&pv_done[s], 1);
         }
+        mbar_init(o_done, 1);
+        mbar_init(o_final, 1);
         fence_barrier_init();
     }
+    if (warp == 5) {
+        tmem_alloc(tmem_holder, kPfTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    const uint32_t S_col[2] = {tmem, tmem + 64};
+    const uint32_t O_col = tmem + 128;
 
-    if (warp == kConsumerWarps) {
+    if (warp == 4) {
+        // ------------------------------------------------ producer
         if (lane == 0) {
-            prefetch_tmap(&tmap);
+            prefetch_tmap(&tm_kv);
+            prefetch_tmap(&tm_q);
+            mbar_arrive_expect_tx(q_full, L::Q_BYTES);
+#pragma unroll
+            for (int h = 0; h < HALVES; ++h)
+                tma_load_3d(sm + L::Q_OFF + h * (L::Q_BYTES / HALVES), &tm_q, q_full, h * 64, t.kv_head * G,
+                            t.q_begin);
             const int npages = (t.length + P - 1) / P;
-            uint32_t it = 0;
-            for (int kt = kt0; kt < kt1; ++kt, ++it) {
-                const int s = it % a.stages;
-                const uint32_t use = it / a.stages;
-                if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, a.err, kErrWaitEmpty)) break;
-                uint8_t *st = smem + (size_t)s * a.stage_bytes;
-                mbar_arrive_expect_tx(&full[s], a.stage_bytes);
+            for (int j = 0; j < nt; ++j) {
+                const int s = j & 1;
+                const uint32_t use = j >> 1;
+                int rows[4];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int pi = kt * 4 + j;
-                    const int row0 = pi < npages ? a.pages[t.kv_base + pi] * 2 * P : a.oob_row;
-#pragma unroll
-                    for (int kv = 0; kv < 2; ++kv)
-#pragma unroll
-                        for (int h = 0; h < HALVES; ++h)
-                            tma_load_3d(st + (kv * HALVES + h) * BLOCK + j * BOX, &tmap, &full[s], h * 64,
-                                        row0 + (pi < npages ? kv * P : 0), t.kv_head);
+                for (int pg = 0; pg < 4; ++pg) {
+                    const int pi = (kt0 + j) * 4 + pg;
+                    rows[pg] = pi < npages ? a.pages[t.kv_base + pi] * 2 * P : -1;
                 }
+                if (use > 0 && !mbar_wait(&k_empty[s], (use - 1) & 1, a.err, kErrWaitEmpty)) break;
+                uint8_t *kd = sm + L::K_OFF + s * L::KV_BYTES;
+                mbar_arrive_expect_tx(&k_full[s], L::KV_BYTES);
+#pragma unroll
+                for (int pg = 0; pg < 4; ++pg)
+#pragma unroll
+                    for (int h = 0; h < HALVES; ++h)
+                        tma_load_3d(kd + h * (L::KV_BYTES / HALVES) + pg * 2048, &tm_kv, &k_full[s], h * 64,
+                                    rows[pg] >= 0 ? rows[pg] : a.oob_row, t.kv_head);
+                if (use > 0 && !mbar_wait(&v_empty[s], (use - 1) & 1, a.err, kErrWaitEmpty)) break;
+                uint8_t *vd = sm + L::V_OFF + s * L::KV_BYTES;
+                mbar_arrive_expect_tx(&v_full[s], L::KV_BYTES);
+#pragma unroll
+                for (int pg = 0; pg < 4; ++pg)
+#pragma unroll
+                    for (int h = 0; h < HALVES; ++h)
+                        tma_load_3d(vd + h * (L::KV_BYTES / HALVES) + pg * 2048, &tm_kv, &v_full[s], h * 64,
+                                    rows[pg] >= 0 ? rows[pg] + P : a.oob_row, t.kv_head);
             }
-            const uint32_t issued = it;
-            for (uint32_t k = issued > (uint32_t)a.stages ? issued - a.stages : 0; k < issued; ++k)
-                if (!mbar_wait(&empty[k % a.stages], (k / a.stages) & 1, a.err, kErrWaitDrain)) break;
         }
-        return;
-    }
-
-    // ---------------- consumers ----------------
-    const int gid = lane >> 2;
-    const int tid4 = lane & 3;
-    const int Hq = a.num_qo_heads;
-    const int m0r = warp * 16 + gid, m1r = m0r + 8;   // this thread's two query rows
-    const int tok0 = m0r % BQ, tok1 = m1r % BQ;
-    const int hd0 = t.kv_head * G + m0r / BQ, hd1 = t.kv_head * G + m1r / BQ;
-    const bool live0 = tok0 < t.n_q, live1 = tok1 < t.n_q;
-    const int p0 = t.pos0 + tok0, p1 = t.pos0 + tok1;
-    const int hi0 = a.causal ? p0 : t.length - 1, hi1 = a.causal ? p1 : t.length - 1;
-    const int lo0 = a.window_left >= 0 ? max(0, p0 - a.window_left) : 0;
-    const int lo1 = a.window_left >= 0 ? max(0, p1 - a.window_left) : 0;
-
-    uint32_t qa[KS][4];
-    {
-        const __nv_bfloat16 *q0 = a.q + ((size_t)(t.q_begin + tok0) * Hq + hd0) * D;
-        const __nv_bfloat16 *q1 = a.q + ((size_t)(t.q_begin + tok1) * Hq + hd1) * D;
+    } else if (warp == 5) {
+        // ------------------------------------------------ MMA issue (one thread) + V tails
+        constexpr uint32_t ID_S = idesc_bf16_f32(128, kPfKeys, 0, 0);
+        constexpr uint32_t ID_O = idesc_bf16_f32(128, D, 0, 1);
+        const uint32_t sQ = smem_u32(sm + L::Q_OFF);
+        const uint32_t tail_begin = t.length;
+        const uint32_t tail_end = ((t.length + P - 1) / P) * P;
+        bool ok = mbar_wait(q_full, 0, a.err, kErrWaitFull);
+        auto issue_pv = [&](int i) {
+            const int s = i & 1;
+            ok = ok && mbar_wait(&p_full[s], (i >> 1) & 1, a.err, kErrWaitFull);
+            ok = ok && mbar_wait(&v_full[s], (i >> 1) & 1, a.err, kErrWaitFull);
+            if (!ok) return;
+            uint8_t *vs = sm + L::V_OFF + s * L::KV_BYTES;
+            // zero V rows of the row's last page past its end (poisoned or stale slots)
+            const int key0 = (kt0 + i) * kPfKeys;
+            const int zb = max((int)tail_begin, key0), ze = min((int)tail_end, key0 + kPfKeys);
+            if (zb < ze) {
+                const int nz = (ze - zb) * (D / 8);
+                for (int e = lane; e < nz; e += 32) {
+                    const int k = zb - key0 + e / (D / 8);
+                    const int chunk = e % (D / 8);
+                    *reinterpret_cast<uint4 *>(vs + (chunk >> 3) * (L::KV_BYTES / HALVES) + swz128(k, chunk & 7)) =
+                        make_uint4(0, 0, 0, 0);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t sV = smem_u32(vs);
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-            const int c0 = ks * 16 + tid4 * 2;
-            qa[ks][0] = live0 ? *reinterpret_cast<const uint32_t *>(q0 + c0) : 0u;
-            qa[ks][2] = live0 ? *reinterpret_cast<const uint32_t *>(q0 + c0 + 8) : 0u;
-            qa[ks][1] = live1 ? *reinterpret_cast<const uint32_t *>(q1 + c0) : 0u;
-            qa[ks][3] = live1 ? *reinterpret_cast<const uint32_t *>(q1 + c0 + 8) : 0u;
-        }
-    }
-    const int k_tok = (lane & 7) + ((lane >> 4) << 3);
-    const int k_chk = (lane >> 3) & 1;
-    const int v_tok = (lane & 7) + (((lane >> 3) & 1) << 3);
-    const int v_chk = lane >> 4;
-
-    float acc[NT][4];
-#pragma unroll
-    for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    const int tail_begin = t.length;                          // first key past the row
-    const int tail_end = ((t.length + P - 1) / P) * P;        // end of the row's last page
-
-    uint32_t it = 0;
-    for (int kt = kt0; kt < kt1; ++kt, ++it) {
-        const int s = it % a.stages;
-        if (!mbar_wait(&full[s], (it / a.stages) & 1, a.err, kErrWaitFull)) return;
-        uint8_t *st = smem + (size_t)s * a.stage_bytes;
-        const uint32_t kb = smem_u32(st);
-        const uint32_t vb = kb + HALVES * BLOCK;
-        const int key0 = kt * KEYS;
-        // zero the V slots of the row's last page past its end (every warp writes the
-        // same zeros, then reads only after its own writes)
-        const int zb = max(tail_begin, key0), ze = min(tail_end, key0 + KEYS);
-        const bool zeroed = zb < ze;
-        if (zeroed) {
-            const int nz = (ze - zb) * (D / 8);
-            for (int i = lane; i < nz; i += 32) {
-                const int k = zb - key0 + i / (D / 8);
-                const int chunk = i % (D / 8);
-                *reinterpret_cast<uint4 *>(st + HALVES * BLOCK + (chunk >> 3) * BLOCK + swz128(k, chunk & 7)) =
-                    make_uint4(0, 0, 0, 0);
+                for (int kk = 0; kk < kPfKeys / 16; ++kk) {
+                    const uint64_t bd = smem_desc(sV + kk * 2048, L::KV_BYTES / HALVES, 1024, kSwizzle128B);
+                    mma_ts(O_col, S_col[s] + kk * 8, bd, ID_O, (i > 0 || kk > 0) ? 1u : 0u);
+                }
+                mma_commit(o_done);
+                mma_commit(&v_empty[s]);
+                mma_commit(&pv_done[s]);
             }
             __syncwarp();
-        }
-        float sc[8][4];
+        };
+        for (int j = 0; j < nt && ok; ++j) {
+            const int s = j & 1;
+            ok = mbar_wait(&k_full[s], (j >> 1) & 1, a.err, kErrWaitFull);
+            // S_j overwrites the columns that PV_{j-2} reads as its A operand (P_{j-2}); MMAs
+            // with different accumulators are not ordered for us, so wait for PV_{j-2}
+            if (ok && j >= 2) ok = mbar_wait(&pv_done[s], ((j - 2) >> 1) & 1, a.err, kErrWaitFull);
+            if (!ok) break;
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t sK = smem_u32(sm + L::K_OFF + s * L::KV_BYTES);
 #pragma unroll
-        for (int n = 0; n < 8; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-            const int chunk = ks * 2 + k_chk;
-#pragma unroll
-            for (int np = 0; np < 4; ++np) {
-                const uint32_t addr = kb + (chunk >> 3) * BLOCK + swz128(np * 16 + k_tok, chunk & 7);
-                uint32_t b0, b1, b2, b3;
-                ldmatrix_x4(addr, b0, b1, b2, b3);
-                mma_bf16_16816(sc[2 * np], qa[ks], b0, b1);
-                mma_bf16_16816(sc[2 * np + 1], qa[ks], b2, b3);
+                for (int kk = 0; kk < KSTEPS; ++kk) {
+                    const uint32_t off = (kk % 4) * 32;  // 16 columns = 32 bytes along the swizzled row
+                    const uint64_t ad = smem_desc(sQ + (kk / 4) * (L::Q_BYTES / HALVES) + off, 16, 1024, kSwizzle128B);
+                    const uint64_t bd =
+                        smem_desc(sK + (kk / 4) * (L::KV_BYTES / HALVES) + off, 16, 1024, kSwizzle128B);
+                    mma_ss(S_col[s], ad, bd, ID_S, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(&s_full[s]);
+                mma_commit(&k_empty[s]);
             }
+            __syncwarp();
+            if (j >= 1) issue_pv(j - 1);
         }
-        float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-        for (int n = 0; n < 8; ++n)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int kp = key0 + n * 8 + tid4 * 2 + e;
-                const bool v0 = kp >= lo0 && kp <= hi0 && kp < t.length;
-                const bool v1 = kp >= lo1 && kp <= hi1 && kp < t.length;
-                sc[n][e] = v0 ? sc[n][e] * a.scale_log2 : -INFINITY;
-                sc[n][e + 2] = v1 ? sc[n][e + 2] * a.scale_log2 : -INFINITY;
-                mx0 = fmaxf(mx0, sc[n][e]);
-                mx1 = fmaxf(mx1, sc[n][e + 2]);
+        if (ok && nt >= 1) issue_pv(nt - 1);
+        if (ok && lane == 0) mma_commit(o_final);
+    } else {
+        // ------------------------------------------------ softmax + epilogue (warps 0-3)
+        const int m = threadIdx.x;  // query row = TMEM lane
+        const int tok = m / G;
+        const int hd = t.kv_head * G + m % G;
+        const bool live = tok < t.n_q;
+        const int pos = t.pos0 + tok;
+        const int hi = a.causal ? pos : t.length - 1;
+        const int lo = a.window_left >= 0 ? max(0, pos - a.window_left) : 0;
+        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        const float sl = a.scale_log2;
+        float m_run = -INFINITY, l_run = 0.f;
+        bool ok = true;
+        for (int j = 0; j < nt; ++j) {
+            const int s = j & 1;
+            const int key0 = (kt0 + j) * kPfKeys;
+            if (!mbar_wait(&s_full[s], (j >> 1) & 1, a.err, kErrWaitFull)) {
+                ok = false;
+                break;
             }
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const float r0 = mn0 == -INFINITY ? 0.f : mn0;
-        const float r1 = mn1 == -INFINITY ? 0.f : mn1;
-        const float al0 = fast_exp2(m0 - r0), al1 = fast_exp2(m1 - r1);
-        m0 = mn0;
-        m1 = mn1;
-        float ps0 = 0.f, ps1 = 0.f;
+            tc_fence_after();
+            uint32_t r0[32], r1[32];
+            tmem_ld32(S_col[s] + lane_off, r0);
+            tmem_ld32(S_col[s] + lane_off + 32, r1);
+            tmem_wait_ld();
+            float sv[64];
 #pragma unroll
-        for (int n = 0; n < 8; ++n)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                sc[n][e] = fast_exp2(sc[n][e] - r0);
-                sc[n][e + 2] = fast_exp2(sc[n][e + 2] - r1);
-                ps0 += sc[n][e];
-                ps1 += sc[n][e + 2];
+            for (int c = 0; c < 32; ++c) {
+                sv[c] = __uint_as_float(r0[c]);
+                sv[32 + c] = __uint_as_float(r1[c]);
             }
-        l0 = l0 * al0 + ps0;
-        l1 = l1 * al1 + ps1;
+            if (key0 < lo || key0 + kPfKeys - 1 > hi || key0 + kPfKeys > t.length) {
 #pragma unroll
-        for (int n = 0; n < NT; ++n) {
-            acc[n][0] *= al0;
-            acc[n][1] *= al0;
-            acc[n][2] *= al1;
-            acc[n][3] *= al1;
+                for (int c = 0; c < 64; ++c) {
+                    const int k = key0 + c;
+                    sv[c] = (k >= lo && k <= hi && k < t.length) ? sv[c] : -INFINITY;
+                }
+            }
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 64; ++c) mx = fmaxf(mx, sv[c]);
+            const float m_tile = mx * sl;  // -inf when the whole tile is masked for this row
+            // move the running max only when it grows by more than the threshold
+            const bool grow = m_tile > m_run + kRescaleThreshold;
+            const bool warp_grow = __any_sync(0xffffffffu, grow) && j > 0;
+            float alpha = 1.f;
+            if (j == 0 || warp_grow) {
+                const float m_new = fmaxf(m_run, m_tile);
+                if (m_new != -INFINITY) {
+                    alpha = exp2f(m_run - m_new);  // 0 when m_run = -inf
+                    m_run = m_new;
+                }
+            }
+            const float mref = m_run == -INFINITY ? 0.f : m_run;
+            float psum = 0.f;
+            uint32_t pk[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                const float p0 = exp2f(fmaf(sv[2 * c], sl, -mref));
+                const float p1 = exp2f(fmaf(sv[2 * c + 1], sl, -mref));
+                psum += p0 + p1;
+                pk[c] = pack_bf16(p0, p1);
+            }
+            l_run = l_run * alpha + psum;
+            tmem_st32(S_col[s] + lane_off, pk);
+            tmem_wait_st();
+            if (warp_grow) {
+                // O holds P_0..P_{j-1} V: wait for the last of those MMAs, then scale O rows
+                if (!mbar_wait(o_done, (j - 1) & 1, a.err, kErrWaitFull)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll 1
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(O_col + lane_off + c0, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+                    tmem_st32(O_col + lane_off + c0, o);
+                }
+                tmem_wait_st();
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&p_full[s]);
         }
+        // epilogue
+        if (ok && mbar_wait(o_final, 0, a.err, kErrWaitFull)) {
+            tc_fence_after();
+            const float inv = 1.f / l_run;
+            __nv_bfloat16 *orow = a.out + ((size_t)(t.q_begin + tok) * a.num_qo_heads + hd) * D;
+#pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                uint32_t o[32];
+                tmem_ld32(O_col + lane_off + c0, o);
+                tmem_wait_ld();
+                uint32_t pkd[16];
 #pragma unroll
-        for (int kk = 0; kk < KEYS / 16; ++kk) {
-            uint32_t pa[4];
-            pa[0] = pack_bf16(sc[2 * kk][0], sc[2 * kk][1]);
-            pa[1] = pack_bf16(sc[2 * kk][2], sc[2 * kk][3]);
-            pa[2] = pack_bf16(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
-            pa[3] = pack_bf16(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
+                for (int c = 0; c < 16; ++c)
+                    pkd[c] = pack_bf16(__uint_as_float(o[2 * c]) * inv, __uint_as_float(o[2 * c + 1]) * inv);
+                if (live) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c0);
 #pragma unroll
-            for (int dj = 0; dj < D / 16; ++dj) {
-                const int chunk = dj * 2 + v_chk;
-                const uint32_t addr = vb + (chunk >> 3) * BLOCK + swz128(kk * 16 + v_tok, chunk & 7);
-                uint32_t b0, b1, b2, b3;
-                ldmatrix_x4_trans(addr, b0, b1, b2, b3);
-                mma_bf16_16816(acc[2 * dj], pa, b0, b1);
-                mma_bf16_16816(acc[2 * dj + 1], pa, b2, b3);
+                    for (int c = 0; c < 4; ++c)
+                        dst[c] = make_uint4(pkd[4 * c], pkd[4 * c + 1], pkd[4 * c + 2], pkd[4 * c + 3]);
+                }
             }
+            if (live && a.lse)
+                a.lse[(size_t)(t.q_begin + tok) * a.num_qo_heads + hd] = (m_run + __log2f(l_run)) * kLn2f;
         }
-        if (zeroed) fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
     }
-
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-    const float inv0 = 1.f / l0, inv1 = 1.f / l1;
-    __nv_bfloat16 *o0 = a.out + ((size_t)(t.q_begin + tok0) * Hq + hd0) * D;
-    __nv_bfloat16 *o1 = a.out + ((size_t)(t.q_begin + tok1) * Hq + hd1) * D;
-#pragma unroll
-    for (int n = 0; n < NT; ++n) {
-        const int c = n * 8 + tid4 * 2;
-        if (live0) *reinterpret_cast<uint32_t *>(o0 + c) = pack_bf16(acc[n][0] * inv0, acc[n][1] * inv0);
-        if (live1) *reinterpret_cast<uint32_t *>(o1 + c) = pack_bf16(acc[n][2] * inv1, acc[n][3] * inv1);
-    }
-    if (a.lse && tid4 == 0) {
-        if (live0) a.lse[(size_t)(t.q_begin + tok0) * Hq + hd0] = (m0 + __log2f(l0)) * kLn2f;
-        if (live1) a.lse[(size_t)(t.q_begin + tok1) * Hq + hd1] = (m1 + __log2f(l1)) * kLn2f;
-    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 5) tmem_dealloc(tmem, kPfTmemCols);
 }
 
 }  // namespace dev
 
-static uint32_t prefill_stage_bytes(const Shape &s) {
-    return (uint32_t)kPrefillKeysPerStage * 2u * (uint32_t)s.head_dim * 2u;
-}
-static int prefill_stages(const Shape &s) {
-    int st = (int)((192u * 1024u) / prefill_stage_bytes(s));
-    return st > 6 ? 6 : st;
-}
 size_t prefill_smem_bytes(const Shape &s) {
-    return 1024 + (size_t)prefill_stages(s) * prefill_stage_bytes(s) + 2 * 8 * 8;
+    // at least 100 KB, so that no more than two CTAs (2 x 256 TMEM columns) share an SM
+    const size_t need = 1024 + (s.head_dim == 64 ? dev::PfSmem<64>::BYTES : dev::PfSmem<128>::BYTES);
+    return need < 100 * 1024 ? 100 * 1024 : need;
 }
 
 template <int D, int G>
-static cudaError_t launch_prefill_t(const CUtensorMap &tm, const dev::PrefillArgs &a, int grid, size_t smem,
-                                    cudaStream_t st) {
-    auto fn = dev::prefill_kernel<D, G>;
+static cudaError_t launch_prefill_t(const CUtensorMap &tkv, const CUtensorMap &tq, const dev::PrefillArgs &a,
+                                    int grid, size_t smem, cudaStream_t st) {
+    auto fn = dev::prefill_tc_kernel<D, G>;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    fn<<<grid, (dev::kConsumerWarps + 1) * 32, smem, st>>>(tm, a);
+    fn<<<grid, dev::kPfThreads, smem, st>>>(tkv, tq, a);
     return cudaGetLastError();
 }
 
-cudaError_t launch_prefill(const Shape &s, const Plan &p, const CUtensorMap &tm, void *ws, const void *q, void *out,
-                           float *lse, cudaStream_t st) {
+cudaError_t launch_prefill(const Shape &s, const Plan &p, const CUtensorMap &tm_kv, const CUtensorMap &tm_q, void *ws,
+                           void *out, float *lse, cudaStream_t st) {
     if (p.pf_tiles == 0) return cudaSuccess;
     uint8_t *w = static_cast<uint8_t *>(ws);
     dev::PrefillArgs a;
-    a.q = static_cast<const __nv_bfloat16 *>(q);
     a.out = static_cast<__nv_bfloat16 *>(out);
     a.lse = lse;
     a.tiles = reinterpret_cast<const PrefillTile *>(w + p.lay.pf_tiles);
@@ -301,8 +383,6 @@ cudaError_t launch_prefill(const Shape &s, const Plan &p, const CUtensorMap &tm,
     a.num_qo_heads = s.num_qo_heads;
     a.page_size = s.page_size;
     a.oob_row = s.num_cache_pages * 2 * s.page_size;
-    a.stages = prefill_stages(s);
-    a.stage_bytes = prefill_stage_bytes(s);
     a.causal = p.causal;
     a.window_left = p.window_left;
     a.scale_log2 = p.sm_scale * 1.4426950408889634f;
@@ -310,7 +390,7 @@ cudaError_t launch_prefill(const Shape &s, const Plan &p, const CUtensorMap &tm,
     cudaError_t e = cudaErrorInvalidValue;
     const int g = s.group();
 #define PKV_PF(DD, GG) \
-    if (s.head_dim == DD && g == GG) e = launch_prefill_t<DD, GG>(tm, a, p.pf_tiles, smem, st);
+    if (s.head_dim == DD && g == GG) e = launch_prefill_t<DD, GG>(tm_kv, tm_q, a, p.pf_tiles, smem, st);
     PKV_PF(64, 1) PKV_PF(64, 2) PKV_PF(64, 4) PKV_PF(64, 8) PKV_PF(64, 16)
     PKV_PF(128, 1) PKV_PF(128, 2) PKV_PF(128, 4) PKV_PF(128, 8) PKV_PF(128, 16)
 #undef PKV_PF

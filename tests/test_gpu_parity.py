@@ -207,3 +207,29 @@ def test_mixed_full_size():
 def test_long_decode_full_size(window):
     pb = wl.config_long(window_left=window)
     _check_step(pb, "decode", window_left=window, unused="randn")
+
+
+# ------------------------------------------------------------------ determinism (races show up here)
+
+@pytest.mark.parametrize("mode", ["decode", "prefill", "mixed"])
+def test_repeated_runs_are_bit_identical(mode):
+    if mode == "decode":
+        lens = list(np.random.default_rng(40).integers(1, 3000, size=60))
+        pb = wl.custom(40, lens, [1] * len(lens), num_qo_heads=32, num_kv_heads=8, head_dim=128, page_size=16)
+    elif mode == "prefill":
+        n = list(np.random.default_rng(41).integers(1, 400, size=12))
+        c = list(np.random.default_rng(42).integers(0, 700, size=12))
+        pb = wl.custom(41, np.add(n, c), n, num_qo_heads=32, num_kv_heads=8, head_dim=128, page_size=16)
+    else:
+        n = [1, 1, 300, 1, 1, 77, 1]
+        c = [900, 40, 20, 1, 2000, 300, 5]
+        pb = _mixed_batch(43, n, c)
+    x = wl.make_inputs(pb, device="cuda", seed=13, unused="nan", layers=1)
+    out0, lse0, h, ws = G.gpu_step(pb, x, mode)
+    for _ in range(4):
+        out = torch.full_like(out0, float("nan"))
+        lse = torch.full_like(lse0, float("nan"))
+        getattr(h, "run_" + mode)(x["q"], x["kv_cache"][0], out, lse, workspace=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), out0.view(torch.int16))
+        assert torch.equal(lse, lse0)
