@@ -45,7 +45,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", choices=["batch", "long", "long_window", "tiny"], default="batch")
+    ap.add_argument("--config", choices=["batch", "long", "long_window", "tiny", "prefill", "mixed"], default="batch",
+                    help="batch (default): the decode step; prefill / mixed: those steps' own lines")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-secondary", action="store_true", help="skip the prefill / mixed / long-decode lines")
     ap.add_argument("--no-e2e", action="store_true")
@@ -349,6 +350,67 @@ def run_ours(args, rank, world):
     return line
 
 
+def run_step_primary(args, rank, world):
+    """--config prefill | mixed: one step = append + the attention pass on one layer slice,
+    timed per step with a 256 MB L2 flush between steps (the slice is ~0.2-1.8 GB)."""
+    from paged_kv_attention_gqa_gb300 import binding as B
+    B.load()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.current_stream()
+    peaks = measured_peaks()
+    pb = wl.config_prefill(seed=args.seed) if args.config == "prefill" else wl.config_mixed(seed=args.seed)
+    mode = B.MODE_PREFILL if args.config == "prefill" else B.MODE_MIXED
+    x = wl.make_inputs(pb, device=dev, seed=args.seed, unused="randn")
+    kv = x["kv_cache"][0]
+    h = make_handle(pb, B)
+    ws = torch.empty(h.workspace_size(mode), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(x["q"])
+    lse = torch.empty(x["q"].shape[:2], dtype=torch.float32, device=dev)
+    run = h.run_prefill if mode == B.MODE_PREFILL else h.run_mixed
+    h.plan(mode, pb.qo_indptr, pb.kv_indptr, pb.kv_indices, pb.last_page_len, workspace=ws)
+    flush = l2_flush_buffer(dev)
+    step_ms, run_ms = [], []
+    for it in range(max(args.warmup, 3) + args.steps):
+        flush.fill_(1)
+        a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        a.record(stream)
+        h.kv_append(x["k_new"], x["v_new"], kv, workspace=ws)
+        b.record(stream)
+        run(x["q"], kv, out, lse, workspace=ws)
+        c.record(stream)
+        torch.cuda.synchronize()
+        if it >= max(args.warmup, 3):
+            step_ms.append(a.elapsed_time(c))
+            run_ms.append(b.elapsed_time(c))
+    assert h.check_device_error(ws) == 0
+    ms = max_over_ranks(statistics.median(step_ms), world)
+    kms = statistics.median(run_ms)
+    if args.config == "prefill":
+        fl = prefill_flops(pb)
+        value, unit = world * fl / (ms * 1e-3) / 1e12, "TFLOP/s"
+        achieved = fl / (kms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": None, "kernel": "prefill_tc_kernel",
+                "launch_ms": round(kms, 5), "peak_source": peaks["source"]}
+        launches = 2
+    else:
+        dec = [r for r in range(pb.batch) if pb.qo_lens[r] == 1]
+        dec_bytes = sum(int(pb.kv_lens[r]) for r in dec) * pb.num_kv_heads * pb.head_dim * 4
+        value, unit = world * dec_bytes / (ms * 1e-3) / 1e9, "GB/s"
+        roof = {"bound": "hbm", "achieved": round(dec_bytes / (kms * 1e-3) / 1e9, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(dec_bytes / (kms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4), "traffic": None,
+                "kernel": "decode pass + prefill pass (run_mixed)", "launch_ms": round(kms, 5),
+                "peak_source": peaks["source"]}
+        launches = 4
+    return {"metric": METRIC, "value": round(value, 2), "unit": unit, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; N(0,1) bf16 q/K/V)",
+            "config": {"workload": f"{pb.name}: {pb.batch} rows, {pb.num_tokens} new tokens, Hq {pb.num_qo_heads} / "
+                                   f"Hkv {pb.num_kv_heads}, head_dim {pb.head_dim}, page_size {pb.page_size}",
+                       "l2": "256 MB written between steps"},
+            "e2e": None, "gpu_launches": launches * args.steps, "roofline": roof}
+
+
 def l2_flush_buffer(dev):
     return torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
@@ -499,7 +561,7 @@ def main():
         if rank == 0:
             print(json.dumps(run_reference(args, rank, world)), flush=True)
         return
-    line = run_ours(args, rank, world)
+    line = run_step_primary(args, rank, world) if args.config in ("prefill", "mixed") else run_ours(args, rank, world)
     if rank == 0:
         print(json.dumps(line), flush=True)
 

@@ -290,34 +290,35 @@ __global__ void __launch_bounds__(9 * 32, 1)
 }
 
 // Merge the split-KV partials of each cut row: with w_j = exp(lse_j - max lse),
-// o = sum_j w_j o_j / sum_j w_j and lse = max lse + ln sum_j w_j.
+// o = sum_j w_j o_j / sum_j w_j and lse = max lse + ln sum_j w_j.  Grid: (cut rows,
+// head groups); one thread per (head, 4 columns).
+constexpr int kMergeHeadsPerCta = 8;
+
 __global__ void __launch_bounds__(256) merge_kernel(const MergeRow *rows, const float *part_o, const float *part_lse,
                                                     __nv_bfloat16 *out, float *lse, int Hq, int D) {
     const MergeRow mr = rows[blockIdx.x];
     if (mr.out_token < 0) return;
     const int per_head = D / 4;
-    for (int e = threadIdx.x; e < Hq * per_head; e += blockDim.x) {
-        const int h = e / per_head;
-        const int c = (e % per_head) * 4;
-        float M = -INFINITY;
-        for (int j = 0; j < mr.count; ++j) M = fmaxf(M, part_lse[(size_t)(mr.first + j) * Hq + h]);
-        float wsum = 0.f;
-        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int j = 0; j < mr.count; ++j) {
-            const float w = __expf(part_lse[(size_t)(mr.first + j) * Hq + h] - M);
-            const float4 v = *reinterpret_cast<const float4 *>(part_o + ((size_t)(mr.first + j) * Hq + h) * D + c);
-            wsum += w;
-            o.x += w * v.x;
-            o.y += w * v.y;
-            o.z += w * v.z;
-            o.w += w * v.w;
-        }
-        const float inv = 1.f / wsum;
-        __nv_bfloat16 *dst = out + ((size_t)mr.out_token * Hq + h) * D + c;
-        *reinterpret_cast<uint32_t *>(dst) = pack_bf16(o.x * inv, o.y * inv);
-        *reinterpret_cast<uint32_t *>(dst + 2) = pack_bf16(o.z * inv, o.w * inv);
-        if (lse && c == 0) lse[(size_t)mr.out_token * Hq + h] = M + __logf(wsum);
+    const int h = blockIdx.y * kMergeHeadsPerCta + threadIdx.x / per_head;
+    const int c = (threadIdx.x % per_head) * 4;
+    if (h >= Hq || threadIdx.x >= kMergeHeadsPerCta * per_head) return;
+    float M = -INFINITY;
+    for (int j = 0; j < mr.count; ++j) M = fmaxf(M, part_lse[(size_t)(mr.first + j) * Hq + h]);
+    float wsum = 0.f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < mr.count; ++j) {
+        const float w = __expf(part_lse[(size_t)(mr.first + j) * Hq + h] - M);
+        const float4 v = *reinterpret_cast<const float4 *>(part_o + ((size_t)(mr.first + j) * Hq + h) * D + c);
+        wsum += w;
+        o.x += w * v.x;
+        o.y += w * v.y;
+        o.z += w * v.z;
+        o.w += w * v.w;
     }
+    const float inv = 1.f / wsum;
+    __nv_bfloat16 *dst = out + ((size_t)mr.out_token * Hq + h) * D + c;
+    *reinterpret_cast<uint2 *>(dst) = make_uint2(pack_bf16(o.x * inv, o.y * inv), pack_bf16(o.z * inv, o.w * inv));
+    if (lse && c == 0) lse[(size_t)mr.out_token * Hq + h] = M + __logf(wsum);
 }
 
 // Last-page append: one warp per new token copies its K and V rows (num_kv_heads x D
@@ -399,7 +400,9 @@ cudaError_t launch_decode(const Shape &s, const Plan &p, const CUtensorMap &tm, 
 #undef PKV_DEC
     if (e != cudaSuccess) return e;
     if (p.num_merge) {
-        dev::merge_kernel<<<p.num_merge, 256, 0, st>>>(reinterpret_cast<const MergeRow *>(w + p.lay.merge_rows),
+        const dim3 mgrid(p.num_merge, (s.num_qo_heads + dev::kMergeHeadsPerCta - 1) / dev::kMergeHeadsPerCta);
+        dev::merge_kernel<<<mgrid, dev::kMergeHeadsPerCta * s.head_dim / 4, 0, st>>>(
+            reinterpret_cast<const MergeRow *>(w + p.lay.merge_rows),
                                                         a.part_o, a.part_lse, a.out, lse, s.num_qo_heads,
                                                         s.head_dim);
         e = cudaGetLastError();

@@ -271,9 +271,18 @@ __global__ void __launch_bounds__(kPfThreads, 2)
                     sv[c] = (k >= lo && k <= hi && k < t.length) ? sv[c] : -INFINITY;
                 }
             }
-            float mx = -INFINITY;
+            float mx;
+            {
+                float a0 = sv[0], a1 = sv[1], a2 = sv[2], a3 = sv[3];
 #pragma unroll
-            for (int c = 0; c < 64; ++c) mx = fmaxf(mx, sv[c]);
+                for (int c = 4; c < 64; c += 8) {
+                    a0 = max3f(a0, sv[c], sv[c + 1]);
+                    a1 = max3f(a1, sv[c + 2], sv[c + 3]);
+                    a2 = max3f(a2, sv[c + 4], sv[c + 5]);
+                    a3 = max3f(a3, sv[c + 6], sv[c + 7]);
+                }
+                mx = max3f(fmaxf(a0, a1), a2, a3);
+            }
             const float m_tile = mx * sl;  // -inf when the whole tile is masked for this row
             // move the running max only when it grows by more than the threshold
             const bool grow = m_tile > m_run + kRescaleThreshold;
@@ -282,20 +291,26 @@ __global__ void __launch_bounds__(kPfThreads, 2)
             if (j == 0 || warp_grow) {
                 const float m_new = fmaxf(m_run, m_tile);
                 if (m_new != -INFINITY) {
-                    alpha = exp2f(m_run - m_new);  // 0 when m_run = -inf
+                    alpha = ex2_ftz(m_run - m_new);  // 0 when m_run = -inf
                     m_run = m_new;
                 }
             }
             const float mref = m_run == -INFINITY ? 0.f : m_run;
-            float psum = 0.f;
+            // p = 2^(s * sl - mref), two columns per packed FMA; sums in four packed chains
+            const uint64_t sl2 = f2_make(sl, sl), nm2 = f2_make(-mref, -mref);
+            uint64_t acc[4] = {0, 0, 0, 0};
             uint32_t pk[32];
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
-                const float p0 = exp2f(fmaf(sv[2 * c], sl, -mref));
-                const float p1 = exp2f(fmaf(sv[2 * c + 1], sl, -mref));
-                psum += p0 + p1;
+                float x0, x1;
+                f2_split(ffma2(f2_make(sv[2 * c], sv[2 * c + 1]), sl2, nm2), x0, x1);
+                const float p0 = ex2_ftz(x0), p1 = ex2_ftz(x1);
+                acc[c & 3] = fadd2(acc[c & 3], f2_make(p0, p1));
                 pk[c] = pack_bf16(p0, p1);
             }
+            float u0, u1;
+            f2_split(fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3])), u0, u1);
+            const float psum = u0 + u1;
             l_run = l_run * alpha + psum;
             tmem_st32(S_col[s] + lane_off, pk);
             tmem_wait_st();
