@@ -81,6 +81,16 @@ enum { PKV_MODE_DECODE = 0, PKV_MODE_PREFILL = 1, PKV_MODE_MIXED = 2 };
  *   sink_page:        mixed only: a caller-reserved page id holding finite values,
  *                     read (one token) by every non-decode row of the decode pass;
  *                     -1 when no mixed plans are made.
+ *   graph_static:     1 = CUDA-graph mode (the wrappers' accelerator_graph): every plan
+ *                     uses the workspace layout of the handle's maxima and every kernel is
+ *                     launched at the maxima, reading the plan's own counts, causal flag,
+ *                     window and scale from the workspace.  pkv_kv_append / pkv_run_* calls
+ *                     captured once into a CUDA graph then stay valid for every later
+ *                     pkv_plan on the same workspace, as long as q, out, lse, k, v and the
+ *                     layer slices keep their addresses and q / out / k / v are sized for
+ *                     the maxima (max_batch rows for decode, max_total_tokens otherwise).
+ *                     Make one uncaptured call of each kind first (it sets kernel
+ *                     attributes).  0 = launches sized to each plan.
  */
 typedef struct {
     int num_qo_heads;
@@ -94,6 +104,7 @@ typedef struct {
     int max_prefill_rows;
     int sm_count;
     int sink_page;
+    int graph_static;
 } pkv_config;
 
 /*

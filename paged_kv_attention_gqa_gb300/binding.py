@@ -35,7 +35,7 @@ class PkvError(RuntimeError):
 class Config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "num_qo_heads", "num_kv_heads", "head_dim", "page_size", "max_batch", "max_total_tokens",
-        "max_num_pages", "num_cache_pages", "max_prefill_rows", "sm_count", "sink_page")]
+        "max_num_pages", "num_cache_pages", "max_prefill_rows", "sm_count", "sink_page", "graph_static")]
 
 
 _lib = None
@@ -102,10 +102,10 @@ class Handle:
     """One pkv handle: static shape and the last plan (see include/pkv.h)."""
 
     def __init__(self, *, num_qo_heads, num_kv_heads, head_dim, page_size, max_batch, max_total_tokens=0,
-                 max_num_pages, num_cache_pages, max_prefill_rows=0, sm_count=0, sink_page=-1):
+                 max_num_pages, num_cache_pages, max_prefill_rows=0, sm_count=0, sink_page=-1, graph_static=0):
         self.lib = load()
         self.cfg = Config(num_qo_heads, num_kv_heads, head_dim, page_size, max_batch, max_total_tokens,
-                          max_num_pages, num_cache_pages, max_prefill_rows, sm_count, sink_page)
+                          max_num_pages, num_cache_pages, max_prefill_rows, sm_count, sink_page, int(graph_static))
         h = ctypes.c_void_p()
         st = self.lib.pkv_create(ctypes.byref(self.cfg), ctypes.byref(h))
         if st != OK:

@@ -40,14 +40,13 @@ struct DecodeArgs {
     const int32_t *pages;
     float *part_o;
     float *part_lse;
-    int *err;
+    PlanHeader *hdr;  // per-plan values (error word, sm_scale) in the workspace
     int num_qo_heads;
     int num_kv_heads;
     int page_size;
     int stages;
     uint32_t stage_bytes;
     uint32_t box_bytes;
-    float scale_log2;  // sm_scale * log2(e)
 };
 
 constexpr float kLn2 = 0.6931471805599453f;
@@ -69,6 +68,9 @@ __global__ void __launch_bounds__(9 * 32, 1)
     const int P = a.page_size;
     const int t_begin = a.cta_ptr[blockIdx.x];
     const int t_end = a.cta_ptr[blockIdx.x + 1];
+    if (t_begin >= t_end) return;  // an idle CTA of a launch at the handle's maxima
+    int *err = &a.hdr->err;
+    const float scale_log2 = a.hdr->scale_log2;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < a.stages; ++s) {
@@ -90,7 +92,7 @@ __global__ void __launch_bounds__(9 * 32, 1)
                 for (int pi = t.page_begin; pi < t.page_begin + t.page_count; ++pi, ++it) {
                     const int s = it % a.stages;
                     const uint32_t use = it / a.stages;
-                    if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, a.err, kErrWaitEmpty)) {
+                    if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, err, kErrWaitEmpty)) {
                         ok = false;
                         break;
                     }
@@ -109,7 +111,7 @@ __global__ void __launch_bounds__(9 * 32, 1)
             const uint32_t issued = it;
             for (uint32_t k = issued > (uint32_t)a.stages ? issued - a.stages : 0; k < issued; ++k) {
                 const int s = k % a.stages;
-                if (!mbar_wait(&empty[s], (k / a.stages) & 1, a.err, kErrWaitDrain)) break;
+                if (!mbar_wait(&empty[s], (k / a.stages) & 1, err, kErrWaitDrain)) break;
             }
         }
         return;
@@ -151,7 +153,7 @@ __global__ void __launch_bounds__(9 * 32, 1)
 
         for (int pi = t.page_begin; pi < t.page_begin + t.page_count; ++pi, ++it) {
             const int s = it % a.stages;
-            if (!mbar_wait(&full[s], (it / a.stages) & 1, a.err, kErrWaitFull)) return;
+            if (!mbar_wait(&full[s], (it / a.stages) & 1, err, kErrWaitFull)) return;
             uint8_t *st = smem + (size_t)s * a.stage_bytes;
             const uint32_t kbase = smem_u32(st);
             const uint32_t vbase = kbase + HALVES * a.box_bytes;
@@ -190,8 +192,8 @@ __global__ void __launch_bounds__(9 * 32, 1)
                 for (int e = 0; e < 2; ++e) {
                     const int pos = pos0 + n * 8 + tid4 * 2 + e;
                     const bool vis = pos >= t.lo && pos < t.length;
-                    sc[n][e] = vis ? sc[n][e] * a.scale_log2 : -INFINITY;
-                    sc[n][e + 2] = vis ? sc[n][e + 2] * a.scale_log2 : -INFINITY;
+                    sc[n][e] = vis ? sc[n][e] * scale_log2 : -INFINITY;
+                    sc[n][e + 2] = vis ? sc[n][e + 2] * scale_log2 : -INFINITY;
                     mx0 = fmaxf(mx0, sc[n][e]);
                     mx1 = fmaxf(mx1, sc[n][e + 2]);
                 }
@@ -294,8 +296,10 @@ __global__ void __launch_bounds__(9 * 32, 1)
 // head groups); one thread per (head, 4 columns).
 constexpr int kMergeHeadsPerCta = 8;
 
-__global__ void __launch_bounds__(256) merge_kernel(const MergeRow *rows, const float *part_o, const float *part_lse,
-                                                    __nv_bfloat16 *out, float *lse, int Hq, int D) {
+__global__ void __launch_bounds__(256) merge_kernel(const PlanHeader *hdr, const MergeRow *rows, const float *part_o,
+                                                    const float *part_lse, __nv_bfloat16 *out, float *lse, int Hq,
+                                                    int D) {
+    if ((int)blockIdx.x >= hdr->num_merge) return;
     const MergeRow mr = rows[blockIdx.x];
     if (mr.out_token < 0) return;
     const int per_head = D / 4;
@@ -323,10 +327,10 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeRow *rows, const 
 
 // Last-page append: one warp per new token copies its K and V rows (num_kv_heads x D
 // bf16 each) to slot rows[t] of the layer slice viewed as [pages * 2 * page_size] rows.
-__global__ void __launch_bounds__(256) append_kernel(const uint4 *k, const uint4 *v, uint4 *cache, const int32_t *rows,
-                                                     int num_tokens, int vec_per_token, int page_size) {
+__global__ void __launch_bounds__(256) append_kernel(const PlanHeader *hdr, const uint4 *k, const uint4 *v, uint4 *cache,
+                                                     const int32_t *rows, int vec_per_token, int page_size) {
     const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (t >= num_tokens) return;
+    if (t >= hdr->num_append) return;
     const size_t row = (size_t)rows[t];
     const int lane = threadIdx.x & 31;
     const uint4 *ks = k + (size_t)t * vec_per_token;
@@ -358,11 +362,19 @@ size_t decode_smem_bytes(const Shape &s) {
     return 1024 + (size_t)decode_stages(s) * decode_stage_bytes(s) + 2 * 8 * 8;
 }
 
+// Raise a kernel's dynamic shared-memory limit; skipped while `st` is being captured
+// into a CUDA graph (a launch before the capture has set it already).
+cudaError_t set_smem_limit(const void *fn, size_t smem, cudaStream_t st) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) == cudaSuccess && cs != cudaStreamCaptureStatusNone) return cudaSuccess;
+    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+}
+
 template <int D, int G>
 static cudaError_t launch_decode_t(const CUtensorMap &tm, const dev::DecodeArgs &a, int grid, int warps, size_t smem,
                                    cudaStream_t st) {
     auto fn = dev::decode_kernel<D, G>;
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = set_smem_limit((const void *)fn, smem, st);
     if (e != cudaSuccess) return e;
     fn<<<grid, warps * 32, smem, st>>>(tm, a);
     return cudaGetLastError();
@@ -370,7 +382,9 @@ static cudaError_t launch_decode_t(const CUtensorMap &tm, const dev::DecodeArgs 
 
 cudaError_t launch_decode(const Shape &s, const Plan &p, const CUtensorMap &tm, void *ws, const void *q, void *out,
                           float *lse, cudaStream_t st) {
-    if (p.dec_ctas == 0) return cudaSuccess;
+    const StaticCounts sc = static_counts(s, p.mode);
+    const int grid = s.graph_static ? sc.dec_ctas : p.dec_ctas;
+    if (grid == 0) return cudaSuccess;
     uint8_t *w = static_cast<uint8_t *>(ws);
     dev::DecodeArgs a;
     a.q = static_cast<const __nv_bfloat16 *>(q);
@@ -381,28 +395,28 @@ cudaError_t launch_decode(const Shape &s, const Plan &p, const CUtensorMap &tm, 
     a.pages = reinterpret_cast<const int32_t *>(w + p.lay.dec_pages);
     a.part_o = reinterpret_cast<float *>(w + p.lay.part_o);
     a.part_lse = reinterpret_cast<float *>(w + p.lay.part_lse);
-    a.err = reinterpret_cast<int *>(w + p.lay.err);
+    a.hdr = reinterpret_cast<PlanHeader *>(w + p.lay.err);
     a.num_qo_heads = s.num_qo_heads;
     a.num_kv_heads = s.num_kv_heads;
     a.page_size = s.page_size;
     a.stages = decode_stages(s);
     a.stage_bytes = decode_stage_bytes(s);
     a.box_bytes = (uint32_t)s.page_size * s.num_kv_heads * 128u;
-    a.scale_log2 = p.sm_scale * 1.4426950408889634f;
     const int warps = s.num_kv_heads + 1;
     const size_t smem = decode_smem_bytes(s);
     cudaError_t e = cudaErrorInvalidValue;
     const int g = s.group();
 #define PKV_DEC(DD, GG) \
-    if (s.head_dim == DD && g == GG) e = launch_decode_t<DD, GG>(tm, a, p.dec_ctas, warps, smem, st);
+    if (s.head_dim == DD && g == GG) e = launch_decode_t<DD, GG>(tm, a, grid, warps, smem, st);
     PKV_DEC(64, 1) PKV_DEC(64, 2) PKV_DEC(64, 4) PKV_DEC(64, 8) PKV_DEC(64, 16)
     PKV_DEC(128, 1) PKV_DEC(128, 2) PKV_DEC(128, 4) PKV_DEC(128, 8) PKV_DEC(128, 16)
 #undef PKV_DEC
     if (e != cudaSuccess) return e;
-    if (p.num_merge) {
-        const dim3 mgrid(p.num_merge, (s.num_qo_heads + dev::kMergeHeadsPerCta - 1) / dev::kMergeHeadsPerCta);
+    const int merges = s.graph_static ? sc.num_merge : p.num_merge;
+    if (merges) {
+        const dim3 mgrid(merges, (s.num_qo_heads + dev::kMergeHeadsPerCta - 1) / dev::kMergeHeadsPerCta);
         dev::merge_kernel<<<mgrid, dev::kMergeHeadsPerCta * s.head_dim / 4, 0, st>>>(
-            reinterpret_cast<const MergeRow *>(w + p.lay.merge_rows),
+            a.hdr, reinterpret_cast<const MergeRow *>(w + p.lay.merge_rows),
                                                         a.part_o, a.part_lse, a.out, lse, s.num_qo_heads,
                                                         s.head_dim);
         e = cudaGetLastError();
@@ -412,14 +426,16 @@ cudaError_t launch_decode(const Shape &s, const Plan &p, const CUtensorMap &tm, 
 
 cudaError_t launch_append(const Shape &s, const Plan &p, void *ws, const void *k, const void *v, void *kv_layer,
                           cudaStream_t st) {
-    if (p.num_append == 0) return cudaSuccess;
+    const int tokens = s.graph_static ? static_counts(s, p.mode).tokens : p.num_append;
+    if (tokens == 0) return cudaSuccess;
     uint8_t *w = static_cast<uint8_t *>(ws);
     const int vec = s.num_kv_heads * s.head_dim * 2 / 16;
     const int warps_per_block = 8;
-    const int grid = (p.num_append + warps_per_block - 1) / warps_per_block;
+    const int grid = (tokens + warps_per_block - 1) / warps_per_block;
     dev::append_kernel<<<grid, warps_per_block * 32, 0, st>>>(
-        static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), static_cast<uint4 *>(kv_layer),
-        reinterpret_cast<const int32_t *>(w + p.lay.append_rows), p.num_append, vec, s.page_size);
+        reinterpret_cast<const PlanHeader *>(w + p.lay.err), static_cast<const uint4 *>(k),
+        static_cast<const uint4 *>(v), static_cast<uint4 *>(kv_layer),
+        reinterpret_cast<const int32_t *>(w + p.lay.append_rows), vec, s.page_size);
     return cudaGetLastError();
 }
 

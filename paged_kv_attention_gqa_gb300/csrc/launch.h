@@ -8,6 +8,7 @@
 namespace pkv {
 
 int decode_stages(const Shape &s);
+cudaError_t set_smem_limit(const void *fn, size_t smem, cudaStream_t st);
 size_t decode_smem_bytes(const Shape &s);
 size_t prefill_smem_bytes(const Shape &s);
 

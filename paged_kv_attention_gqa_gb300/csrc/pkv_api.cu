@@ -68,6 +68,7 @@ extern "C" pkv_status pkv_create(const pkv_config *cfg, pkv_handle_t *out) {
         return fail(nullptr, PKV_ERR_UNSUPPORTED, "num_kv_heads above 8 is not computed");
     if (c.sink_page >= c.num_cache_pages)
         return fail(nullptr, PKV_ERR_INVALID, "sink_page outside the cache");
+    if (c.graph_static != 0 && c.graph_static != 1) return fail(nullptr, PKV_ERR_INVALID, "graph_static is 0 or 1");
     if ((long long)c.num_cache_pages * 2 * c.page_size >= (1ll << 31))
         return fail(nullptr, PKV_ERR_UNSUPPORTED, "cache has too many pages for 32-bit slot rows");
     int sms = c.sm_count;
@@ -80,7 +81,7 @@ extern "C" pkv_status pkv_create(const pkv_config *cfg, pkv_handle_t *out) {
     pkv_handle_t h = new pkv_handle_s();
     h->shape = Shape{c.num_qo_heads, c.num_kv_heads, c.head_dim,       c.page_size, c.max_batch,
                      c.max_total_tokens, c.max_num_pages, c.num_cache_pages, c.max_prefill_rows,
-                     sms,             c.sink_page};
+                     sms,             c.sink_page,      c.graph_static};
     *out = h;
     return PKV_OK;
 }
@@ -216,6 +217,12 @@ static pkv_status q_map(pkv_handle_t h, const void *q, int rows) {
     return PKV_OK;
 }
 
+// Rows of q the tensor map covers: the plan's tokens, or the maxima in graph mode (a
+// captured launch keeps the map it was captured with).
+static int q_rows(pkv_handle_t h) {
+    return h->shape.graph_static ? h->shape.max_total_tokens : h->plan.num_tokens;
+}
+
 static pkv_status check_planned(pkv_handle_t h, void *ws, int mode_a, int mode_b = -1) {
     if (!h) return PKV_ERR_INVALID;
     if (!h->planned_ws || h->planned_ws != ws)
@@ -277,7 +284,7 @@ extern "C" pkv_status pkv_run_prefill(pkv_handle_t h, const void *q, const void 
     if (h->plan.num_tokens == 0) return PKV_OK;
     if ((st = check_io(h, q, kv_layer, out)) != PKV_OK) return st;
     if ((st = pf_map(h, kv_layer)) != PKV_OK) return st;
-    if ((st = q_map(h, q, h->plan.num_tokens)) != PKV_OK) return st;
+    if ((st = q_map(h, q, q_rows(h))) != PKV_OK) return st;
     cudaError_t e = pkv::launch_prefill(h->shape, h->plan, h->tm_pf, h->tm_q, workspace, out, lse,
                                         static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PKV_OK : cuda_fail(h, e, "prefill launch");
@@ -291,7 +298,7 @@ extern "C" pkv_status pkv_run_mixed(pkv_handle_t h, const void *q, const void *k
     if ((st = check_io(h, q, kv_layer, out)) != PKV_OK) return st;
     if ((st = dec_map(h, kv_layer)) != PKV_OK) return st;
     if ((st = pf_map(h, kv_layer)) != PKV_OK) return st;
-    if ((st = q_map(h, q, h->plan.num_tokens)) != PKV_OK) return st;
+    if ((st = q_map(h, q, q_rows(h))) != PKV_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = pkv::launch_decode(h->shape, h->plan, h->tm_dec, workspace, q, out, lse, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "mixed decode-pass launch");

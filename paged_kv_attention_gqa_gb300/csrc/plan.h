@@ -22,6 +22,21 @@ constexpr int kPrefillRowsPerTile = 128;
 // Keys per prefill K/V stage (4 pages of 16).
 constexpr int kPrefillKeysPerStage = 64;
 
+// First bytes of every plan in the workspace: the per-plan values the kernels read on
+// the device, so that launches captured into a CUDA graph stay valid for later plans
+// (their arguments are only pointers and static shapes).
+struct PlanHeader {
+    int32_t err;          // device error word (bounded waits that gave up)
+    int32_t num_append;   // new tokens
+    int32_t dec_ctas;     // decode CTAs with work
+    int32_t num_merge;    // cut rows to merge
+    int32_t pf_tiles;     // prefill tiles
+    int32_t causal;
+    int32_t window_left;
+    float scale_log2;     // sm_scale * log2(e)
+};
+static_assert(sizeof(PlanHeader) <= kAlign, "the header fits its aligned slot");
+
 // One piece of a row's visible pages handled by one decode CTA.
 struct DecodeTile {
     int32_t q_token;     // token whose query this row uses
@@ -60,7 +75,7 @@ static_assert(sizeof(PrefillTile) == 32, "PrefillTile is 8 ints");
 
 // Byte offsets of the plan's arrays inside the workspace.
 struct PlanLayout {
-    size_t err = 0;            // int32 device error word (+ padding)
+    size_t err = 0;            // PlanHeader (its first word is the device error word)
     size_t append_rows = 0;    // int32[num_append]: page * 2 * page_size + slot of each new token
     size_t dec_pages = 0;      // int32[dec_nnz]: page ids the decode pass reads
     size_t pf_pages = 0;       // int32[pf_nnz]:  page ids the prefill pass reads
@@ -79,8 +94,16 @@ struct Shape {
     int num_qo_heads, num_kv_heads, head_dim, page_size;
     int max_batch, max_total_tokens, max_num_pages, num_cache_pages, max_prefill_rows;
     int sm_count, sink_page;
+    int graph_static;  // launch at the maxima with a fixed workspace layout (CUDA-graph mode)
     int group() const { return num_qo_heads / num_kv_heads; }
 };
+
+// Worst-case counts at a handle's maxima for one plan mode: the launch grids and the
+// workspace layout of graph mode, and the bound pkv_workspace_size reports.
+struct StaticCounts {
+    int tokens, dec_nnz, pf_nnz, dec_tiles, dec_ctas, num_merge, pf_tiles, partials;
+};
+StaticCounts static_counts(const Shape &s, int mode);
 
 // Everything a plan produced, host side.  `image` is the integer part exactly as it is
 // copied to the workspace.

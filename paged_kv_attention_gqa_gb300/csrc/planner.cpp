@@ -324,20 +324,27 @@ static PlanLayout layout_for(const Shape &s, int num_append, int dec_nnz, int pf
     return L;
 }
 
+StaticCounts static_counts(const Shape &s, int mode) {
+    StaticCounts c;
+    const int C = decode_cta_limit(s);
+    const int rows = s.max_batch;
+    const int dec_rows = mode == PKV_MODE_PREFILL ? 0 : rows;
+    c.tokens = mode == PKV_MODE_DECODE ? s.max_batch : s.max_total_tokens;
+    c.dec_nnz = mode == PKV_MODE_DECODE ? s.max_num_pages : (mode == PKV_MODE_MIXED ? s.max_num_pages + rows : 0);
+    c.pf_nnz = mode == PKV_MODE_DECODE ? 0 : s.max_num_pages;
+    c.dec_tiles = dec_rows ? dec_rows + C : 0;
+    c.dec_ctas = dec_rows ? C : 0;
+    c.num_merge = dec_rows ? C : 0;
+    const int pf_rows = mode == PKV_MODE_MIXED ? std::min(rows, s.max_prefill_rows) : rows;
+    c.pf_tiles = mode == PKV_MODE_DECODE ? 0 : prefill_tile_bound(s, pf_rows, c.tokens);
+    c.partials = dec_rows ? dec_rows + C : 0;
+    return c;
+}
+
 size_t workspace_bound(const Shape &s, int mode) {
-    int C = decode_cta_limit(s);
-    int tokens = mode == PKV_MODE_DECODE ? s.max_batch : s.max_total_tokens;
-    int rows = s.max_batch;
-    int dec_rows = mode == PKV_MODE_PREFILL ? 0 : rows;
-    int dec_nnz = mode == PKV_MODE_DECODE ? s.max_num_pages : (mode == PKV_MODE_MIXED ? s.max_num_pages + rows : 0);
-    int pf_nnz = mode == PKV_MODE_DECODE ? 0 : s.max_num_pages;
-    int dec_tiles = dec_rows ? dec_rows + C : 0;
-    int dec_ctas = dec_rows ? C : 0;
-    int num_merge = dec_rows ? C : 0;
-    int pf_rows = mode == PKV_MODE_MIXED ? std::min(rows, s.max_prefill_rows) : rows;
-    int pf_tiles = mode == PKV_MODE_DECODE ? 0 : prefill_tile_bound(s, pf_rows, tokens);
-    int partials = dec_rows ? dec_rows + C : 0;
-    return layout_for(s, tokens, dec_nnz, pf_nnz, dec_tiles, dec_ctas, num_merge, pf_tiles, partials).total;
+    const StaticCounts c = static_counts(s, mode);
+    return layout_for(s, c.tokens, c.dec_nnz, c.pf_nnz, c.dec_tiles, c.dec_ctas, c.num_merge, c.pf_tiles, c.partials)
+        .total;
 }
 
 template <class T>
@@ -424,14 +431,36 @@ int make_plan(const Shape &s, int mode, const int32_t *qo, const int32_t *kvp, c
     plan.num_merge = (int)merges.size();
     plan.num_partials = partials;
     plan.pf_tiles = (int)ptiles.size();
-    plan.lay = layout_for(s, T, plan.dec_nnz, plan.pf_nnz, plan.dec_tiles, plan.dec_ctas, plan.num_merge,
-                          plan.pf_tiles, partials);
+    if (s.graph_static) {
+        // fixed layout at the maxima: captured launches keep pointing at the right arrays;
+        // idle decode CTAs get empty tile ranges
+        const StaticCounts c = static_counts(s, mode);
+        plan.lay = layout_for(s, c.tokens, c.dec_nnz, c.pf_nnz, c.dec_tiles, c.dec_ctas, c.num_merge, c.pf_tiles,
+                              c.partials);
+        if (c.dec_ctas) {
+            if (cta_ptr.empty()) cta_ptr.assign(1, 0);
+            while ((int)cta_ptr.size() < c.dec_ctas + 1) cta_ptr.push_back(cta_ptr.back());
+        }
+    } else {
+        plan.lay = layout_for(s, T, plan.dec_nnz, plan.pf_nnz, plan.dec_tiles, plan.dec_ctas, plan.num_merge,
+                              plan.pf_tiles, partials);
+    }
     plan.image.assign(plan.lay.int_bytes, 0);
+    PlanHeader hdr;
+    hdr.err = 0;
+    hdr.num_append = T;
+    hdr.dec_ctas = plan.dec_ctas;
+    hdr.num_merge = plan.num_merge;
+    hdr.pf_tiles = plan.pf_tiles;
+    hdr.causal = plan.causal;
+    hdr.window_left = window_left;
+    hdr.scale_log2 = plan.sm_scale * 1.4426950408889634f;
+    put(plan.image, plan.lay.err, &hdr, 1);
     put(plan.image, plan.lay.append_rows, app.data(), app.size());
     put(plan.image, plan.lay.dec_pages, dec_pages.data(), dec_pages.size());
     put(plan.image, plan.lay.pf_pages, pf_pages.data(), pf_pages.size());
     put(plan.image, plan.lay.dec_tiles, dtiles.data(), dtiles.size());
-    if (plan.dec_ctas) put(plan.image, plan.lay.dec_cta_ptr, cta_ptr.data(), cta_ptr.size());
+    if (!cta_ptr.empty() && (plan.dec_ctas || s.graph_static)) put(plan.image, plan.lay.dec_cta_ptr, cta_ptr.data(), cta_ptr.size());
     put(plan.image, plan.lay.merge_rows, merges.data(), merges.size());
     put(plan.image, plan.lay.pf_tiles, ptiles.data(), ptiles.size());
     return PKV_OK;

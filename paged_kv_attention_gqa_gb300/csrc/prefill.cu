@@ -38,13 +38,10 @@ struct PrefillArgs {
     float *lse;
     const PrefillTile *tiles;
     const int32_t *pages;
-    int *err;
+    PlanHeader *hdr;  // per-plan values (tile count, causal, window, sm_scale) in the workspace
     int num_qo_heads;
     int page_size;
     int oob_row;  // a row coordinate past the cache: TMA fills it with zeros
-    int causal;
-    int window_left;
-    float scale_log2;
 };
 
 constexpr int kPfThreads = 192;  // warps 0-3 softmax, 4 producer, 5 MMA
@@ -92,7 +89,11 @@ __global__ void __launch_bounds__(kPfThreads, 2)
     uint64_t *o_final = bars + 16;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 17);
 
+    if ((int)blockIdx.x >= a.hdr->pf_tiles) return;  // an idle CTA of a launch at the maxima
     const PrefillTile t = a.tiles[blockIdx.x];
+    int *const err = &a.hdr->err;
+    const int causal = a.hdr->causal;
+    const int window_left = a.hdr->window_left;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int P = a.page_size;
@@ -145,7 +146,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
                     const int pi = (kt0 + j) * 4 + pg;
                     rows[pg] = pi < npages ? a.pages[t.kv_base + pi] * 2 * P : -1;
                 }
-                if (use > 0 && !mbar_wait(&k_empty[s], (use - 1) & 1, a.err, kErrWaitEmpty)) break;
+                if (use > 0 && !mbar_wait(&k_empty[s], (use - 1) & 1, err, kErrWaitEmpty)) break;
                 uint8_t *kd = sm + L::K_OFF + s * L::KV_BYTES;
                 mbar_arrive_expect_tx(&k_full[s], L::KV_BYTES);
 #pragma unroll
@@ -154,7 +155,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
                     for (int h = 0; h < HALVES; ++h)
                         tma_load_3d(kd + h * (L::KV_BYTES / HALVES) + pg * 2048, &tm_kv, &k_full[s], h * 64,
                                     rows[pg] >= 0 ? rows[pg] : a.oob_row, t.kv_head);
-                if (use > 0 && !mbar_wait(&v_empty[s], (use - 1) & 1, a.err, kErrWaitEmpty)) break;
+                if (use > 0 && !mbar_wait(&v_empty[s], (use - 1) & 1, err, kErrWaitEmpty)) break;
                 uint8_t *vd = sm + L::V_OFF + s * L::KV_BYTES;
                 mbar_arrive_expect_tx(&v_full[s], L::KV_BYTES);
 #pragma unroll
@@ -172,11 +173,11 @@ __global__ void __launch_bounds__(kPfThreads, 2)
         const uint32_t sQ = smem_u32(sm + L::Q_OFF);
         const uint32_t tail_begin = t.length;
         const uint32_t tail_end = ((t.length + P - 1) / P) * P;
-        bool ok = mbar_wait(q_full, 0, a.err, kErrWaitFull);
+        bool ok = mbar_wait(q_full, 0, err, kErrWaitFull);
         auto issue_pv = [&](int i) {
             const int s = i & 1;
-            ok = ok && mbar_wait(&p_full[s], (i >> 1) & 1, a.err, kErrWaitFull);
-            ok = ok && mbar_wait(&v_full[s], (i >> 1) & 1, a.err, kErrWaitFull);
+            ok = ok && mbar_wait(&p_full[s], (i >> 1) & 1, err, kErrWaitFull);
+            ok = ok && mbar_wait(&v_full[s], (i >> 1) & 1, err, kErrWaitFull);
             if (!ok) return;
             uint8_t *vs = sm + L::V_OFF + s * L::KV_BYTES;
             // zero V rows of the row's last page past its end (poisoned or stale slots)
@@ -209,10 +210,10 @@ __global__ void __launch_bounds__(kPfThreads, 2)
         };
         for (int j = 0; j < nt && ok; ++j) {
             const int s = j & 1;
-            ok = mbar_wait(&k_full[s], (j >> 1) & 1, a.err, kErrWaitFull);
+            ok = mbar_wait(&k_full[s], (j >> 1) & 1, err, kErrWaitFull);
             // S_j overwrites the columns that PV_{j-2} reads as its A operand (P_{j-2}); MMAs
             // with different accumulators are not ordered for us, so wait for PV_{j-2}
-            if (ok && j >= 2) ok = mbar_wait(&pv_done[s], ((j - 2) >> 1) & 1, a.err, kErrWaitFull);
+            if (ok && j >= 2) ok = mbar_wait(&pv_done[s], ((j - 2) >> 1) & 1, err, kErrWaitFull);
             if (!ok) break;
             tc_fence_after();
             if (lane == 0) {
@@ -240,16 +241,16 @@ __global__ void __launch_bounds__(kPfThreads, 2)
         const int hd = t.kv_head * G + m % G;
         const bool live = tok < t.n_q;
         const int pos = t.pos0 + tok;
-        const int hi = a.causal ? pos : t.length - 1;
-        const int lo = a.window_left >= 0 ? max(0, pos - a.window_left) : 0;
+        const int hi = causal ? pos : t.length - 1;
+        const int lo = window_left >= 0 ? max(0, pos - window_left) : 0;
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-        const float sl = a.scale_log2;
+        const float sl = a.hdr->scale_log2;
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
         for (int j = 0; j < nt; ++j) {
             const int s = j & 1;
             const int key0 = (kt0 + j) * kPfKeys;
-            if (!mbar_wait(&s_full[s], (j >> 1) & 1, a.err, kErrWaitFull)) {
+            if (!mbar_wait(&s_full[s], (j >> 1) & 1, err, kErrWaitFull)) {
                 ok = false;
                 break;
             }
@@ -316,7 +317,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
             tmem_wait_st();
             if (warp_grow) {
                 // O holds P_0..P_{j-1} V: wait for the last of those MMAs, then scale O rows
-                if (!mbar_wait(o_done, (j - 1) & 1, a.err, kErrWaitFull)) {
+                if (!mbar_wait(o_done, (j - 1) & 1, err, kErrWaitFull)) {
                     ok = false;
                     break;
                 }
@@ -337,7 +338,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
             if (lane == 0) mbar_arrive(&p_full[s]);
         }
         // epilogue
-        if (ok && mbar_wait(o_final, 0, a.err, kErrWaitFull)) {
+        if (ok && mbar_wait(o_final, 0, err, kErrWaitFull)) {
             tc_fence_after();
             const float inv = 1.f / l_run;
             __nv_bfloat16 *orow = a.out + ((size_t)(t.q_begin + tok) * a.num_qo_heads + hd) * D;
@@ -379,7 +380,7 @@ template <int D, int G>
 static cudaError_t launch_prefill_t(const CUtensorMap &tkv, const CUtensorMap &tq, const dev::PrefillArgs &a,
                                     int grid, size_t smem, cudaStream_t st) {
     auto fn = dev::prefill_tc_kernel<D, G>;
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = set_smem_limit((const void *)fn, smem, st);
     if (e != cudaSuccess) return e;
     fn<<<grid, dev::kPfThreads, smem, st>>>(tkv, tq, a);
     return cudaGetLastError();
@@ -387,25 +388,23 @@ static cudaError_t launch_prefill_t(const CUtensorMap &tkv, const CUtensorMap &t
 
 cudaError_t launch_prefill(const Shape &s, const Plan &p, const CUtensorMap &tm_kv, const CUtensorMap &tm_q, void *ws,
                            void *out, float *lse, cudaStream_t st) {
-    if (p.pf_tiles == 0) return cudaSuccess;
+    const int grid = s.graph_static ? static_counts(s, p.mode).pf_tiles : p.pf_tiles;
+    if (grid == 0) return cudaSuccess;
     uint8_t *w = static_cast<uint8_t *>(ws);
     dev::PrefillArgs a;
     a.out = static_cast<__nv_bfloat16 *>(out);
     a.lse = lse;
     a.tiles = reinterpret_cast<const PrefillTile *>(w + p.lay.pf_tiles);
     a.pages = reinterpret_cast<const int32_t *>(w + p.lay.pf_pages);
-    a.err = reinterpret_cast<int *>(w + p.lay.err);
+    a.hdr = reinterpret_cast<PlanHeader *>(w + p.lay.err);
     a.num_qo_heads = s.num_qo_heads;
     a.page_size = s.page_size;
     a.oob_row = s.num_cache_pages * 2 * s.page_size;
-    a.causal = p.causal;
-    a.window_left = p.window_left;
-    a.scale_log2 = p.sm_scale * 1.4426950408889634f;
     const size_t smem = prefill_smem_bytes(s);
     cudaError_t e = cudaErrorInvalidValue;
     const int g = s.group();
 #define PKV_PF(DD, GG) \
-    if (s.head_dim == DD && g == GG) e = launch_prefill_t<DD, GG>(tm_kv, tm_q, a, p.pf_tiles, smem, st);
+    if (s.head_dim == DD && g == GG) e = launch_prefill_t<DD, GG>(tm_kv, tm_q, a, grid, smem, st);
     PKV_PF(64, 1) PKV_PF(64, 2) PKV_PF(64, 4) PKV_PF(64, 8) PKV_PF(64, 16)
     PKV_PF(128, 1) PKV_PF(128, 2) PKV_PF(128, 4) PKV_PF(128, 8) PKV_PF(128, 16)
 #undef PKV_PF
