@@ -66,6 +66,7 @@ typedef enum {
 } pkv_status;
 
 enum { PKV_MODE_DECODE = 0, PKV_MODE_PREFILL = 1, PKV_MODE_MIXED = 2 };
+enum { PKV_NON_CAUSAL = 0, PKV_CAUSAL = 1, PKV_CONTEXT_ONLY = 2 };
 
 /*
  * Static configuration, fixed for the life of a handle (the wrappers' constructor
@@ -142,6 +143,13 @@ pkv_status pkv_workspace_size(pkv_handle_t h, int mode, size_t *bytes);
  *   mode          PKV_MODE_DECODE: qo_indptr may be NULL (row r's query is token r);
  *                 PKV_MODE_PREFILL / PKV_MODE_MIXED: qo_indptr required.
  *   causal        prefill and mixed (the prefill pass); decode is always "sees its row".
+ *                 0 non-causal, 1 causal, 2 (PKV_CONTEXT_ONLY, prefill plans only):
+ *                 attention over the stored context alone (mstar.engine.resources.kv.plan,
+ *                 context_only_views): the index arrays describe only the context (see
+ *                 pkv_context_only_views), query i of row r sits at position L_r + i and
+ *                 sees every context key (window_left counted from that position); n_r may
+ *                 exceed L_r; a query that sees no key gets out = 0 and lse = -inf.  Such a
+ *                 plan appends nothing (pkv_kv_append is a no-op on it).
  *   window_left   -1 unbounded, else >= 0.
  *   sm_scale      0 selects 1/sqrt(head_dim).
  *   workspace     device buffer of workspace_bytes (>= pkv_workspace_size for the
@@ -243,6 +251,19 @@ pkv_status pkv_mixed_layout(const int32_t *qo_indptr, const int32_t *paged_kv_in
                             int32_t *perm, int32_t *pf_qo_indptr, int32_t *dec_kv_indptr,
                             int32_t *dec_kv_indices, int32_t *dec_last_page_len, int32_t *dec_q_token,
                             int32_t *dec_out_token, int *dec_nnz);
+
+/*
+ * mstar.engine.resources.kv.plan, context_only_views: the views of a step without the
+ * tokens it appends.  Row r's length shrinks by its query count n_r = qo_indptr[r+1] -
+ * qo_indptr[r]; the pages past the shorter length are dropped; last_page_len is
+ * recomputed (0 for a row left without context).  Outputs: out_kv_indptr[batch+1],
+ * out_kv_indices (<= input nnz entries), out_last_page_len[batch]; *out_nnz receives the
+ * number of indices written.  PKV_ERR_INVALID if a row has more queries than tokens.
+ */
+pkv_status pkv_context_only_views(int page_size, const int32_t *qo_indptr, const int32_t *paged_kv_indptr,
+                                  const int32_t *paged_kv_indices, const int32_t *paged_kv_last_page_len, int batch,
+                                  int32_t *out_kv_indptr, int32_t *out_kv_indices, int32_t *out_last_page_len,
+                                  int *out_nnz);
 
 /*
  * The decode work split the plan would make: tiles[k] = {row, first visible page,

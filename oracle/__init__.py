@@ -118,7 +118,8 @@ def attention(q_bits, kv_layer_bits, qo_indptr, kv_indptr, kv_indices, last_page
         mask[chunk] = 1
         rc = lib.oracle_attention(_ptr(q_bits), _ptr(kv), max_pages, _ptr(qo), _ptr(kvp), _ptr(kvi),
                                   _ptr(lpl), batch, num_qo_heads, num_kv_heads, head_dim, page_size,
-                                  int(bool(causal)), int(window_left), float(sm_scale), _ptr(mask),
+                                  int(causal if causal == 2 else bool(causal)), int(window_left), float(sm_scale),
+                                  _ptr(mask),
                                   _ptr(out), _ptr(lse))
         if rc != 0:
             errors.append(rc)

@@ -62,12 +62,35 @@ def append_slots(qo_indptr, kv_indptr, kv_indices, last_page_len, page_size: int
     return pages, slots
 
 
-def visible_range(length: int, num_new: int, i: int, causal: bool, window_left: int):
-    """Inclusive key range [lo, hi] that new token i of a row sees."""
-    p = length - num_new + i
-    hi = p if causal else length - 1
+def visible_range(length: int, num_new: int, i: int, causal, window_left: int):
+    """Inclusive key range [lo, hi] that new token i of a row sees (empty when hi < lo).
+    causal: True / 1 causal, False / 0 non-causal, 2 context-only (the queries follow the
+    row's `length` stored tokens)."""
+    p = length + i if causal == 2 else length - num_new + i
+    hi = p if causal is True or causal == 1 else length - 1
     lo = max(0, p - window_left) if window_left >= 0 else 0
     return lo, hi
+
+
+def context_only_views(qo_indptr, kv_indptr, kv_indices, last_page_len, page_size: int):
+    """mstar.engine.resources.kv.plan, context_only_views: each row's length shrinks by its
+    query count (to_compute), the pages past the shorter length are dropped and the last
+    page's fill is recomputed.  Returns (kv_indptr, kv_indices, last_page_len); a row left
+    with no context has no pages and last_page_len 0."""
+    qo = np.asarray(qo_indptr, dtype=np.int64)
+    kvp = np.asarray(kv_indptr, dtype=np.int64)
+    kvi = np.asarray(kv_indices, dtype=np.int64)
+    L = row_lengths(kv_indptr, last_page_len, page_size)
+    new_p, new_i, new_l = [0], [], []
+    for r in range(len(kvp) - 1):
+        ctx = int(L[r]) - int(qo[r + 1] - qo[r])
+        assert ctx >= 0, "a row cannot append more tokens than its length"
+        keep = -(-ctx // page_size)
+        new_i.extend(int(x) for x in kvi[kvp[r]: kvp[r] + keep])
+        new_p.append(len(new_i))
+        new_l.append(last_page_len_of(ctx, page_size) if ctx > 0 else 0)
+    i32 = lambda x: np.asarray(x, dtype=np.int32)
+    return i32(new_p), i32(new_i), i32(new_l)
 
 
 def mixed_layout(qo_indptr, kv_indptr, kv_indices, last_page_len, *, max_prefill_rows: int,

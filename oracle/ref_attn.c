@@ -23,9 +23,15 @@
  *
  *   Visibility (FlashInferPrefillWrapper.plan, the window_left sentence; causal
  *   alignment "attend to the cached prefix plus themselves"):
- *     causal:      keys j with lo <= j <= p
- *     non-causal:  keys j with lo <= j <= L_r - 1
+ *     causal (1):        keys j with lo <= j <= p
+ *     non-causal (0):    keys j with lo <= j <= L_r - 1
+ *     context-only (2):  the row's pages hold only the stored context, the queries come
+ *                        after it (mstar.engine.resources.kv.plan, context_only_views:
+ *                        "length shrinks by to_compute ... to_compute becomes the row's
+ *                        query count"): query i sits at p = L_r + i and sees keys
+ *                        lo <= j <= L_r - 1; n_r may exceed L_r.
  *     lo = max(0, p - window_left) when window_left >= 0, else 0.
+ *     A query that sees no key (an empty context) gets o = 0 and lse = -inf.
  *
  *   Attention (the textbook softmax definition the wrappers compute):
  *     s_j = sm_scale * <q, K_j>;  m = max_j s_j;  l = sum_j exp(s_j - m);
@@ -90,14 +96,14 @@ int oracle_attention(const uint16_t *q, const uint16_t *kv_layer, int64_t max_pa
         int L = row_length(kv_indptr, last_page_len, r, page_size);
         int n = qo_indptr[r + 1] - qo_indptr[r];
         if (n == 0) continue;
-        if (L < n) return -1;
-        int c = L - n;
+        if (causal != 2 && L < n) return -1;
+        int c = causal == 2 ? L : L - n;
 
         /* Gather the row's pages into contiguous K and V: [L, num_kv_heads, head_dim]. */
-        size_t row_elems = (size_t)L * num_kv_heads * head_dim;
+        size_t row_elems = (size_t)(L > 0 ? L : 1) * num_kv_heads * head_dim;
         float *K = (float *)malloc(row_elems * sizeof(float));
         float *V = (float *)malloc(row_elems * sizeof(float));
-        float *s = (float *)malloc((size_t)L * sizeof(float));
+        float *s = (float *)malloc((size_t)(L > 0 ? L : 1) * sizeof(float));
         if (!K || !V || !s) { free(K); free(V); free(s); return -3; }
         for (int p = 0; p < L; ++p) {
             int64_t page = kv_indices[kv_indptr[r] + p / page_size];
@@ -116,13 +122,18 @@ int oracle_attention(const uint16_t *q, const uint16_t *kv_layer, int64_t max_pa
         for (int i = 0; i < n; ++i) {
             int t = qo_indptr[r] + i;
             int p = c + i;
-            int hi = causal ? p : L - 1;
+            int hi = causal == 1 ? p : L - 1;
             int lo = 0;
             if (window_left >= 0) lo = p - window_left > 0 ? p - window_left : 0;
             for (int h = 0; h < num_qo_heads; ++h) {
                 int hk = h / group;
                 const uint16_t *qv = q + ((size_t)t * num_qo_heads + h) * head_dim;
                 float *o = out + ((size_t)t * num_qo_heads + h) * head_dim;
+                if (hi < lo) {
+                    for (int d = 0; d < head_dim; ++d) o[d] = 0.0f;
+                    if (lse) lse[(size_t)t * num_qo_heads + h] = -INFINITY;
+                    continue;
+                }
                 float m = -INFINITY;
                 for (int j = lo; j <= hi; ++j) {
                     const float *kj = K + ((size_t)j * num_kv_heads + hk) * head_dim;

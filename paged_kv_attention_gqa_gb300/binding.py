@@ -17,12 +17,13 @@ LIB_PATH = os.path.join(_PKG, "libpkv.so")
 
 OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_TOO_MANY_PREFILL_ROWS, ERR_NOT_PLANNED, ERR_CUDA, ERR_DEVICE = range(8)
 MODE_DECODE, MODE_PREFILL, MODE_MIXED = 0, 1, 2
+NON_CAUSAL, CAUSAL, CONTEXT_ONLY = 0, 1, 2
 STATUS_NAMES = ["OK", "INVALID", "UNSUPPORTED", "WORKSPACE", "TOO_MANY_PREFILL_ROWS", "NOT_PLANNED", "CUDA", "DEVICE"]
 
 # every symbol include/pkv.h declares
 EXPORTS = ["pkv_create", "pkv_destroy", "pkv_last_error", "pkv_workspace_size", "pkv_plan", "pkv_kv_append",
            "pkv_run_decode", "pkv_run_prefill", "pkv_run_mixed", "pkv_check_device_error", "pkv_append_slots",
-           "pkv_mixed_layout", "pkv_decode_split", "pkv_run_decode_static"]
+           "pkv_mixed_layout", "pkv_decode_split", "pkv_run_decode_static", "pkv_context_only_views"]
 
 
 class PkvError(RuntimeError):
@@ -65,6 +66,7 @@ def load(path: str = LIB_PATH):
         "pkv_mixed_layout": ([i32p, i32p, i32p, i32p, i, i, i] + [i32p] * 9 + [ctypes.POINTER(i)], i),
         "pkv_decode_split": ([vp, i32p, i32p, i, i, i32p, ctypes.POINTER(i), ctypes.POINTER(i)], i),
         "pkv_run_decode_static": ([vp, vp, vp, vp, vp, i32p, i32p, i32p, i, i, ctypes.c_float, vp], i),
+        "pkv_context_only_views": ([i, i32p, i32p, i32p, i32p, i, i32p, i32p, i32p, ctypes.POINTER(i)], i),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -138,7 +140,8 @@ class Handle:
         arrs = [_i32(qo_indptr), _i32(kv_indptr), _i32(kv_indices), _i32(last_page_len)]
         batch = len(arrs[1]) - 1
         self._keep = arrs  # host arrays are read synchronously; kept only for symmetry
-        st = self.lib.pkv_plan(self.h, mode, *(_p(a) for a in arrs), batch, int(bool(causal)), int(window_left),
+        st = self.lib.pkv_plan(self.h, mode, *(_p(a) for a in arrs), batch,
+                               int(causal) if causal == CONTEXT_ONLY else int(bool(causal)), int(window_left),
                                float(sm_scale), _dptr(workspace), workspace.numel() * workspace.element_size(),
                                _stream(stream))
         self._check(st)
@@ -186,6 +189,19 @@ def append_slots(page_size, qo_indptr, kv_indptr, kv_indices, last_page_len):
     if st != OK:
         raise PkvError(st, "append_slots")
     return pages, slots
+
+
+def context_only_views(page_size, qo_indptr, kv_indptr, kv_indices, last_page_len):
+    lib = load()
+    qo, kvp, kvi, lpl = _i32(qo_indptr), _i32(kv_indptr), _i32(kv_indices), _i32(last_page_len)
+    B = len(kvp) - 1
+    okvp, okvi, olpl = np.zeros(B + 1, np.int32), np.zeros(max(len(kvi), 1), np.int32), np.zeros(B, np.int32)
+    nnz = ctypes.c_int()
+    st = lib.pkv_context_only_views(page_size, _p(qo), _p(kvp), _p(kvi), _p(lpl), B, _p(okvp), _p(okvi), _p(olpl),
+                                    ctypes.byref(nnz))
+    if st != OK:
+        raise PkvError(st, "context_only_views")
+    return okvp, okvi[: nnz.value], olpl
 
 
 def mixed_layout(qo_indptr, kv_indptr, kv_indices, last_page_len, *, max_prefill_rows, sink_page):

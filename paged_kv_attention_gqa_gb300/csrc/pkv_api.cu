@@ -335,6 +335,16 @@ extern "C" pkv_status pkv_append_slots(int page_size, const int32_t *qo, const i
     return (pkv_status)pkv::append_slots(page_size, qo, kvp, kvi, lpl, batch, pages, slots, err);
 }
 
+extern "C" pkv_status pkv_context_only_views(int page_size, const int32_t *qo, const int32_t *kvp, const int32_t *kvi,
+                                             const int32_t *lpl, int batch, int32_t *out_kvp, int32_t *out_kvi,
+                                             int32_t *out_lpl, int *out_nnz) {
+    if (!qo || !kvp || !lpl || !out_kvp || !out_lpl || !out_nnz || page_size <= 0 || batch < 0) return PKV_ERR_INVALID;
+    if (kvp[batch] > 0 && (!kvi || !out_kvi)) return PKV_ERR_INVALID;
+    std::string err;
+    return (pkv_status)pkv::context_only_views(page_size, qo, kvp, kvi, lpl, batch, out_kvp, out_kvi, out_lpl, out_nnz,
+                                               err);
+}
+
 extern "C" pkv_status pkv_mixed_layout(const int32_t *qo, const int32_t *kvp, const int32_t *kvi, const int32_t *lpl,
                                        int batch, int max_prefill_rows, int sink_page, int32_t *is_decode,
                                        int32_t *prompt_rows, int32_t *perm, int32_t *pf_qo_indptr,

@@ -127,7 +127,12 @@ struct Plan {
 // Host planner entry points (plain C++, no CUDA).  Each returns 0 on success, else a
 // pkv_status code with `err` explaining it.
 int validate_rows(const Shape &s, int mode, const int32_t *qo, const int32_t *kvp, const int32_t *kvi,
-                  const int32_t *lpl, int batch, int window_left, std::string &err);
+                  const int32_t *lpl, int batch, int window_left, std::string &err, int causal = 1);
+// mstar.engine.resources.kv.plan, context_only_views: drop each row's query tokens from
+// its view (length shrinks by its query count, pages past the new length dropped).
+int context_only_views(int page_size, const int32_t *qo, const int32_t *kvp, const int32_t *kvi, const int32_t *lpl,
+                       int batch, int32_t *out_kvp, int32_t *out_kvi, int32_t *out_lpl, int *out_nnz,
+                       std::string &err);
 int append_slots(int page_size, const int32_t *qo, const int32_t *kvp, const int32_t *kvi, const int32_t *lpl,
                  int batch, int32_t *pages, int32_t *slots, std::string &err);
 struct MixedLayout {

@@ -33,7 +33,11 @@ static int row_len(const int32_t *kvp, const int32_t *lpl, int r, int P) {
 }
 
 int validate_rows(const Shape &s, int mode, const int32_t *qo, const int32_t *kvp, const int32_t *kvi,
-                  const int32_t *lpl, int batch, int window_left, std::string &err) {
+                  const int32_t *lpl, int batch, int window_left, std::string &err, int causal) {
+    if (causal < 0 || causal > 2 || (causal == 2 && mode != PKV_MODE_PREFILL)) {
+        err = "causal is 0, 1, or 2 (context-only, prefill plans only)";
+        return PKV_ERR_INVALID;
+    }
     if (batch < 0 || batch > s.max_batch) {
         err = "batch " + std::to_string(batch) + " outside [0, max_batch=" + std::to_string(s.max_batch) + "]";
         return PKV_ERR_INVALID;
@@ -95,7 +99,7 @@ int validate_rows(const Shape &s, int mode, const int32_t *qo, const int32_t *kv
             err = "decode row " + std::to_string(r) + " has no tokens";
             return PKV_ERR_INVALID;
         }
-        if (n > L) {
+        if (n > L && causal != 2) {
             err = "row " + std::to_string(r) + " has " + std::to_string(n) + " new tokens but length " +
                   std::to_string(L);
             return PKV_ERR_INVALID;
@@ -124,6 +128,25 @@ int append_slots(int P, const int32_t *qo, const int32_t *kvp, const int32_t *kv
             slots[t0 + i] = p % P;
         }
     }
+    return PKV_OK;
+}
+
+int context_only_views(int P, const int32_t *qo, const int32_t *kvp, const int32_t *kvi, const int32_t *lpl,
+                       int batch, int32_t *out_kvp, int32_t *out_kvi, int32_t *out_lpl, int *out_nnz, std::string &err) {
+    int at = 0;
+    out_kvp[0] = 0;
+    for (int r = 0; r < batch; ++r) {
+        const int ctx = row_len(kvp, lpl, r, P) - (qo[r + 1] - qo[r]);
+        if (ctx < 0) {
+            err = "row " + std::to_string(r) + " appends more tokens than its length";
+            return PKV_ERR_INVALID;
+        }
+        const int keep = (ctx + P - 1) / P;
+        for (int i = 0; i < keep; ++i) out_kvi[at++] = kvi[kvp[r] + i];
+        out_kvp[r + 1] = at;
+        out_lpl[r] = ctx > 0 ? (ctx - 1) % P + 1 : 0;
+    }
+    *out_nnz = at;
     return PKV_OK;
 }
 
@@ -264,12 +287,14 @@ static void prefill_tiles(const Shape &s, const std::vector<int> &rows, const in
         int n = qo[r + 1] - qo[r];
         if (n <= 0) continue;
         int L = row_len(kvp, lpl, r, P);
-        int c = L - n;
+        // causal 2 (context-only): the row's pages hold the context; its queries follow it
+        int c = causal == 2 ? L : L - n;
         for (int t0 = 0; t0 < n; t0 += BQ) {
             int nq = std::min(BQ, n - t0);
             int p0 = c + t0, p1 = c + t0 + nq - 1;
             int kb = window_left >= 0 ? std::max(0, p0 - window_left) : 0;
-            int ke = causal ? p1 + 1 : L;
+            int ke = causal == 1 ? p1 + 1 : L;
+            if (ke <= kb) kb = ke = 0;  // no query of the tile sees a key: zeros, lse -inf
             for (int hk = 0; hk < s.num_kv_heads; ++hk) {
                 PrefillTile t;
                 t.q_begin = q_begin_of_row[r] + t0;
@@ -355,23 +380,27 @@ static void put(std::vector<uint8_t> &img, size_t off, const T *src, size_t n) {
 int make_plan(const Shape &s, int mode, const int32_t *qo, const int32_t *kvp, const int32_t *kvi,
               const int32_t *lpl, int batch, int causal, int window_left, float sm_scale, Plan &plan,
               std::string &err) {
-    int rc = validate_rows(s, mode, qo, kvp, kvi, lpl, batch, window_left, err);
+    int rc = validate_rows(s, mode, qo, kvp, kvi, lpl, batch, window_left, err, causal);
     if (rc) return rc;
     plan = Plan();
     plan.mode = mode;
     plan.batch = batch;
-    plan.causal = causal ? 1 : 0;
+    plan.causal = causal;
     plan.window_left = window_left;
     plan.sm_scale = sm_scale > 0.f ? sm_scale : 1.0f / std::sqrt((float)s.head_dim);
     const int T = qo ? qo[batch] : batch;
     plan.num_tokens = T;
-    plan.num_append = T;
+    // a context-only plan's arrays describe the context alone: it appends nothing
+    plan.num_append = causal == 2 ? 0 : T;
     const int P = s.page_size;
 
-    std::vector<int32_t> pages(T), slots(T), app(T);
-    rc = append_slots(P, mode == PKV_MODE_DECODE ? nullptr : qo, kvp, kvi, lpl, batch, pages.data(), slots.data(), err);
-    if (rc) return rc;
-    for (int t = 0; t < T; ++t) app[t] = pages[t] * 2 * P + slots[t];
+    std::vector<int32_t> pages(T), slots(T), app(plan.num_append);
+    if (plan.num_append) {
+        rc = append_slots(P, mode == PKV_MODE_DECODE ? nullptr : qo, kvp, kvi, lpl, batch, pages.data(), slots.data(),
+                          err);
+        if (rc) return rc;
+        for (int t = 0; t < T; ++t) app[t] = pages[t] * 2 * P + slots[t];
+    }
 
     std::vector<DecodeTile> dtiles;
     std::vector<int32_t> cta_ptr;
@@ -448,7 +477,7 @@ int make_plan(const Shape &s, int mode, const int32_t *qo, const int32_t *kvp, c
     plan.image.assign(plan.lay.int_bytes, 0);
     PlanHeader hdr;
     hdr.err = 0;
-    hdr.num_append = T;
+    hdr.num_append = plan.num_append;
     hdr.dec_ctas = plan.dec_ctas;
     hdr.num_merge = plan.num_merge;
     hdr.pf_tiles = plan.pf_tiles;

@@ -241,7 +241,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
         const int hd = t.kv_head * G + m % G;
         const bool live = tok < t.n_q;
         const int pos = t.pos0 + tok;
-        const int hi = causal ? pos : t.length - 1;
+        const int hi = causal == 1 ? pos : t.length - 1;
         const int lo = window_left >= 0 ? max(0, pos - window_left) : 0;
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
         const float sl = a.hdr->scale_log2;
@@ -340,7 +340,8 @@ __global__ void __launch_bounds__(kPfThreads, 2)
         // epilogue
         if (ok && mbar_wait(o_final, 0, err, kErrWaitFull)) {
             tc_fence_after();
-            const float inv = 1.f / l_run;
+            const bool none = l_run == 0.f;  // no visible key (empty context): o = 0, lse = -inf
+            const float inv = none ? 0.f : 1.f / l_run;
             __nv_bfloat16 *orow = a.out + ((size_t)(t.q_begin + tok) * a.num_qo_heads + hd) * D;
 #pragma unroll 1
             for (int c0 = 0; c0 < D; c0 += 32) {
@@ -349,8 +350,8 @@ __global__ void __launch_bounds__(kPfThreads, 2)
                 tmem_wait_ld();
                 uint32_t pkd[16];
 #pragma unroll
-                for (int c = 0; c < 16; ++c)
-                    pkd[c] = pack_bf16(__uint_as_float(o[2 * c]) * inv, __uint_as_float(o[2 * c + 1]) * inv);
+                for (int c = 0; c < 16; ++c)  // select, not multiply: unwritten O may hold NaN bits
+                    pkd[c] = none ? 0u : pack_bf16(__uint_as_float(o[2 * c]) * inv, __uint_as_float(o[2 * c + 1]) * inv);
                 if (live) {
                     uint4 *dst = reinterpret_cast<uint4 *>(orow + c0);
 #pragma unroll
@@ -359,7 +360,8 @@ __global__ void __launch_bounds__(kPfThreads, 2)
                 }
             }
             if (live && a.lse)
-                a.lse[(size_t)(t.q_begin + tok) * a.num_qo_heads + hd] = (m_run + __log2f(l_run)) * kLn2f;
+                a.lse[(size_t)(t.q_begin + tok) * a.num_qo_heads + hd] =
+                    none ? -INFINITY : (m_run + __log2f(l_run)) * kLn2f;
         }
     }
     tc_fence_before();

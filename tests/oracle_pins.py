@@ -25,7 +25,7 @@ from oracle import plan_ref
 from paged_kv_attention_gqa_gb300 import workloads as wl
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
-_ENV = {"e": math.e, "log": math.log, "exp": math.exp}
+_ENV = {"e": math.e, "log": math.log, "exp": math.exp, "inf": math.inf}
 
 
 def closed_form(expr: str) -> float:
@@ -54,7 +54,7 @@ def golden_case_arrays(case):
         qo.append(qo[-1] + row["n_new"])
         kvi.extend(row["pages"])
         kvp.append(len(kvi))
-        lpl.append((L - 1) % P + 1)
+        lpl.append((L - 1) % P + 1 if L else 0)
     q = np.asarray(qs, np.float32).reshape(-1, Hq, D)
     return to_bits(q), to_bits(cache), (np.array(qo), np.array(kvp), np.array(kvi), np.array(lpl))
 
@@ -74,7 +74,10 @@ def pin_golden(lib=None, tol=2e-6):
             got = out[t, h].astype(np.float64)
             assert np.all(np.abs(got - want) <= tol * np.maximum(1, np.abs(want))), (case["name"], t, h, got, want)
             wl_ = closed_form(ex["lse"])
-            assert abs(float(lse[t, h]) - wl_) <= tol * max(1, abs(wl_)), (case["name"], t, h, lse[t, h], wl_)
+            if math.isinf(wl_):
+                assert float(lse[t, h]) == wl_, (case["name"], t, h, lse[t, h], wl_)
+            else:
+                assert abs(float(lse[t, h]) - wl_) <= tol * max(1, abs(wl_)), (case["name"], t, h, lse[t, h], wl_)
 
 
 def build_step(pb, seed=0):
@@ -96,7 +99,8 @@ def build_step(pb, seed=0):
 
 def sdpa_reference(pb, q, kv_layer, *, causal, window_left, sm_scale):
     """float64 attention on unpaged K/V through torch's SDPA (the masks follow the
-    visibility rule; softmax, scaling and the weighted sum are the library's)."""
+    visibility rule; softmax, scaling and the weighted sum are the library's).  A query
+    with no visible key is given o = 0, lse = -inf."""
     T, Hq, D = q.shape
     g = pb.num_qo_heads // pb.num_kv_heads
     out = torch.full((T, Hq, D), float("nan"), dtype=torch.float64)
@@ -106,6 +110,10 @@ def sdpa_reference(pb, q, kv_layer, *, causal, window_left, sm_scale):
         n, L = int(pb.qo_lens[r]), int(pb.kv_lens[r])
         if n == 0:
             continue
+        if L == 0:
+            out[qo[r]: qo[r + 1]] = 0.0
+            lse[qo[r]: qo[r + 1]] = float("-inf")
+            continue
         K, V = wl.logical_kv(pb, kv_layer, r)
         K = K.double().repeat_interleave(g, dim=1).transpose(0, 1)   # [Hq, L, D]
         V = V.double().repeat_interleave(g, dim=1).transpose(0, 1)
@@ -114,9 +122,11 @@ def sdpa_reference(pb, q, kv_layer, *, causal, window_left, sm_scale):
         for i in range(n):
             lo, hi = plan_ref.visible_range(L, n, i, causal, window_left)
             mask[i, lo: hi + 1] = True
-        o = F.scaled_dot_product_attention(Q, K, V, attn_mask=mask, scale=sm_scale)
+        empty = ~mask.any(dim=1)
+        o = F.scaled_dot_product_attention(Q, K, V, attn_mask=mask | empty[:, None], scale=sm_scale)
         s = torch.matmul(Q, K.transpose(1, 2)) * sm_scale
         s = s.masked_fill(~mask, float("-inf"))
+        o[:, empty] = 0.0
         out[qo[r]: qo[r + 1]] = o.transpose(0, 1)
         lse[qo[r]: qo[r + 1]] = torch.logsumexp(s, dim=-1).transpose(0, 1)
     return out, lse
@@ -275,5 +285,32 @@ def pin_append(lib=None):
     assert np.abs(out - ro.numpy()).max() <= 2e-5 and np.abs(lse - rl.numpy()).max() <= 2e-5
 
 
+def context_step(pb, seed=0):
+    """Inputs for context-only attention: every stored position of each row holds K/V
+    (the context) and the rows' queries are drawn separately."""
+    ctx = wl.PagedBatch(pb.name, pb.num_qo_heads, pb.num_kv_heads, pb.head_dim, pb.page_size, pb.kv_lens,
+                        np.zeros_like(pb.qo_lens), pb.page_table, pb.max_pages)
+    x = wl.make_inputs(ctx, seed=seed, unused="nan", layers=1)
+    g = torch.Generator().manual_seed(seed + 1000)
+    q = torch.randn(pb.num_tokens, pb.num_qo_heads, pb.head_dim, generator=g).to(torch.bfloat16)
+    return q, x["kv_cache"][0]
+
+
+def pin_sdpa_context_only(lib=None, tol=2e-5):
+    cases = [([37, 0, 16, 5], [3, 2, 40, 1], 8, 2, 64, 16, -1),
+             ([70, 33, 1], [9, 1, 4], 4, 1, 32, 8, 10),
+             ([64, 3], [64, 70], 8, 8, 16, 4, 0),
+             ([64, 3], [64, 70], 8, 8, 16, 4, 40)]
+    for k, (Ls, ns, Hq, Hkv, D, P, wleft) in enumerate(cases):
+        pb = wl.custom(200 + k, Ls, ns, num_qo_heads=Hq, num_kv_heads=Hkv, head_dim=D, page_size=P)
+        q, kv = context_step(pb, seed=k)
+        out, lse = run_oracle(pb, q, kv, causal=2, window_left=wleft, sm_scale=0.2, lib=lib)
+        ro, rl = sdpa_reference(pb, q, kv, causal=2, window_left=wleft, sm_scale=0.2)
+        assert np.abs(out - ro.numpy()).max() <= tol, k
+        fin = np.isfinite(rl.numpy())
+        assert np.array_equal(fin, np.isfinite(lse)), k
+        assert not fin.any() or np.abs(lse[fin] - rl.numpy()[fin]).max() <= tol, k
+
+
 ALL_PINS = [pin_golden, pin_sdpa, pin_pool_permutation, pin_page_size_invariance, pin_rows_sum_to_one,
-            pin_single_key_cases, pin_decode_is_one_token_prefill, pin_append]
+            pin_single_key_cases, pin_decode_is_one_token_prefill, pin_append, pin_sdpa_context_only]

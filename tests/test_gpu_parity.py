@@ -233,3 +233,44 @@ def test_repeated_runs_are_bit_identical(mode):
         torch.cuda.synchronize()
         assert torch.equal(out.view(torch.int16), out0.view(torch.int16))
         assert torch.equal(lse, lse0)
+
+
+# ------------------------------------------------------------------ context-only attention (causal = 2)
+
+@pytest.mark.parametrize("window", [-1, 0, 5, 100])
+def test_prefill_context_only(window):
+    import oracle_pins
+    from paged_kv_attention_gqa_gb300 import binding as B
+    L = [0, 37, 16, 300, 5, 129, 64]
+    n = [3, 10, 40, 64, 70, 1, 130]
+    pb = wl.custom(60, L, n, num_qo_heads=32, num_kv_heads=8, head_dim=128, page_size=16)
+    q, kv = oracle_pins.context_step(pb, seed=3)
+    x = dict(q=q.cuda(), k_new=None, v_new=None, kv_cache=kv.unsqueeze(0).cuda())
+    out, lse, h, ws = G.gpu_step(pb, x, "prefill", causal=B.CONTEXT_ONLY, window_left=window, append=False)
+    ref_o, ref_l = G.oracle_attn(pb, wl.bf16_bits(q), wl.bf16_bits(kv), causal=2, window_left=window)
+    o, l = out.float().cpu().numpy(), lse.cpu().numpy()
+    empty = ~np.isfinite(ref_l)
+    assert np.array_equal(~np.isfinite(l), empty)
+    assert np.all(o[np.broadcast_to(empty[..., None], o.shape)] == 0)
+    ref_l = np.where(empty, 0, ref_l)
+    l_cmp = torch.from_numpy(np.where(empty, 0, l))
+    G.compare(out, l_cmp, ref_o, ref_l, what=f"context-only window {window}")
+
+
+def test_context_only_views_then_prefill_matches_full_rows_without_their_queries():
+    """A step's rows through pkv_context_only_views: the context-only pass over the shrunk
+    views equals the oracle's context-only attention over the same context."""
+    import oracle_pins
+    from paged_kv_attention_gqa_gb300 import binding as B
+    n = [5, 1, 33, 70]
+    c = [40, 0, 100, 7]
+    full = wl.custom(61, np.add(n, c), n, num_qo_heads=16, num_kv_heads=2, head_dim=64, page_size=16)
+    kvp, kvi, lpl = B.context_only_views(16, *full.index_arrays())
+    table = [kvi[kvp[r]: kvp[r + 1]] for r in range(full.batch)]
+    ctx = wl.PagedBatch("ctx", 16, 2, 64, 16, np.asarray(c), np.asarray(n), table, full.max_pages)
+    assert np.array_equal(ctx.kv_indptr, kvp) and np.array_equal(ctx.last_page_len, lpl)
+    q, kv = oracle_pins.context_step(ctx, seed=4)
+    x = dict(q=q.cuda(), k_new=None, v_new=None, kv_cache=kv.unsqueeze(0).cuda())
+    out, lse, _, _ = G.gpu_step(ctx, x, "prefill", causal=B.CONTEXT_ONLY, append=False)
+    ref_o, ref_l = G.oracle_attn(ctx, wl.bf16_bits(q), wl.bf16_bits(kv), causal=2)
+    G.compare(out, lse, ref_o, ref_l, what="context-only views")

@@ -195,3 +195,25 @@ def test_workspace_bound_holds(lib):
         st, msg = _plan_status(h, mode, (None if mode == 0 else pb.qo_indptr, pb.kv_indptr, pb.kv_indices,
                                          pb.last_page_len), ws_bytes=bound)
         assert st != B.ERR_WORKSPACE, msg
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_context_only_views_bit_exact(lib, seed):
+    rng = np.random.default_rng(300 + seed)
+    Bn = int(rng.integers(1, 30))
+    n = rng.integers(0, 40, size=Bn)
+    c = rng.integers(0, 70, size=Bn)
+    pb = wl.custom(seed, n + c, n, num_qo_heads=8, num_kv_heads=2, head_dim=64, page_size=16)
+    got = B.context_only_views(16, *pb.index_arrays())
+    want = plan_ref.context_only_views(*pb.index_arrays(), 16)
+    for g, w in zip(got, want):
+        assert np.array_equal(g, w)
+    # the views keep exactly the first L - n positions of every row
+    L = plan_ref.row_lengths(got[0], got[2], 16)
+    assert np.array_equal(L, c)
+
+
+def test_context_only_needs_prefill_mode(lib):
+    h = _handle(num_cache_pages=100, max_num_pages=100)
+    st, msg = _plan_status(h, B.MODE_DECODE, (None, [0, 1], [3], [4]), causal=2)
+    assert st == B.ERR_INVALID and "context" in msg

@@ -12,8 +12,11 @@ import oracle_pins as pins
 SRC = open(os.path.join(os.path.dirname(oracle.__file__), "ref_attn.c")).read()
 
 MUTATIONS = {
-    "causal_excludes_self": ("int hi = causal ? p : L - 1;", "int hi = causal ? p - 1 : L - 1;"),
-    "noncausal_drops_last": ("int hi = causal ? p : L - 1;", "int hi = causal ? p : L - 2;"),
+    "causal_excludes_self": ("int hi = causal == 1 ? p : L - 1;", "int hi = causal == 1 ? p - 1 : L - 1;"),
+    "noncausal_drops_last": ("int hi = causal == 1 ? p : L - 1;", "int hi = causal == 1 ? p : L - 2;"),
+    "context_only_query_inside_row": ("int c = causal == 2 ? L : L - n;", "int c = L - n;"),
+    "empty_context_not_zero": ("for (int d = 0; d < head_dim; ++d) o[d] = 0.0f;\n                    if (lse)",
+                               "for (int d = 0; d < head_dim; ++d) o[d] = 1.0f;\n                    if (lse)"),
     "window_one_short": ("lo = p - window_left > 0 ? p - window_left : 0;",
                           "lo = p - window_left + 1 > 0 ? p - window_left + 1 : 0;"),
     "window_ignored": ("if (window_left >= 0) lo", "if (window_left >= 1000000) lo"),
