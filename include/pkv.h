@@ -65,7 +65,7 @@ typedef enum {
     PKV_ERR_DEVICE = 7                 /* a kernel recorded a device-side error (wait limit hit) */
 } pkv_status;
 
-enum { PKV_MODE_DECODE = 0, PKV_MODE_PREFILL = 1, PKV_MODE_MIXED = 2 };
+enum { PKV_MODE_DECODE = 0, PKV_MODE_PREFILL = 1, PKV_MODE_MIXED = 2, PKV_MODE_DENSE = 3 };
 enum { PKV_NON_CAUSAL = 0, PKV_CAUSAL = 1, PKV_CONTEXT_ONLY = 2 };
 
 /*
@@ -195,6 +195,33 @@ pkv_status pkv_run_prefill(pkv_handle_t h, const void *q, const void *kv_layer, 
  */
 pkv_status pkv_run_mixed(pkv_handle_t h, const void *q, const void *kv_layer, void *out, float *lse,
                          void *workspace, pkv_stream_t stream);
+
+/*
+ * Dense varlen attention (mstar.engine.resources.attn.dense, DenseAttentionManager and
+ * DensePlan): one pass over contiguous [frozen prefix | fresh tokens] K/V per segment,
+ * no KV write.  pkv_plan_dense takes HOST int32 cu_q[batch+1] (query offsets into q /
+ * out) and cu_k[batch+1] (key-row offsets into k / v); segment r's queries are its last
+ * n_r = cu_q[r+1]-cu_q[r] keys' tokens (n_r <= L_r = cu_k[r+1]-cu_k[r]), so query i sits at
+ * position L_r - n_r + i; causal 0/1 and window_left as for pkv_plan.  Workspace:
+ * pkv_workspace_size(PKV_MODE_DENSE).  pkv_run_dense: q / out [cu_q[batch], Hq, D] bf16,
+ * k / v [cu_k[batch], Hkv, D] bf16 (device, contiguous, 16-byte aligned), lse
+ * [cu_q[batch], Hq] fp32 or NULL.  The pages call this path eager-only; graph_static does
+ * not apply to it.
+ */
+pkv_status pkv_plan_dense(pkv_handle_t h, const int32_t *cu_q, const int32_t *cu_k, int batch, int causal,
+                          int window_left, float sm_scale, void *workspace, size_t workspace_bytes,
+                          pkv_stream_t stream);
+pkv_status pkv_run_dense(pkv_handle_t h, const void *q, const void *k, const void *v, void *out, float *lse,
+                         void *workspace, pkv_stream_t stream);
+
+/*
+ * Gather a frozen prefix out of the pages (DenseAttentionManager: "gathers the prefix once
+ * per (stream, layer)"): positions 0 .. num_tokens-1 of the page list `pages` (DEVICE
+ * int32, ceil(num_tokens / page_size) ids) are copied from the layer slice into k_out and
+ * v_out ([num_tokens, Hkv, D] bf16, device).  Pure data movement.
+ */
+pkv_status pkv_gather_kv(pkv_handle_t h, const void *kv_layer, const int32_t *pages, int num_tokens, void *k_out,
+                         void *v_out, pkv_stream_t stream);
 
 /*
  * Read and clear the workspace's device error word (synchronises `stream`).

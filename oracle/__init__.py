@@ -8,8 +8,9 @@ no attention arithmetic.
 
 Contents
   ref_attn.c   plain single-threaded fp32 C: gather pages, textbook softmax
-               attention + LSE, last-page append (see its header for the
-               definitions and the page passages they follow).
+               attention + LSE, last-page append, dense varlen attention over
+               contiguous K/V runs (see its header for the definitions and the page
+               passages they follow).
   plan_ref.py  the index work in plain Python: append slots, visible ranges, the
                mixed-step classification, permutation and sink routing.
 
@@ -63,6 +64,8 @@ def load(path: str | None = None):
         lib.oracle_attention.restype = i
         lib.oracle_kv_append.argtypes = [p, ctypes.c_int64, p, p, p, p, p, p, i, i, i, i]
         lib.oracle_kv_append.restype = i
+        lib.oracle_dense_attention.argtypes = [p, p, p, p, p, i, i, i, i, i, i, ctypes.c_float, p, p]
+        lib.oracle_dense_attention.restype = i
         if path is None:
             _lib = lib
     return lib
@@ -150,3 +153,23 @@ def kv_append(kv_layer_bits, k_new_bits, v_new_bits, qo_indptr, kv_indptr, kv_in
     if rc != 0:
         raise ValueError(f"oracle_kv_append rejected its input (code {rc})")
     return kv
+
+
+def dense_attention(q_bits, k_bits, v_bits, cu_q, cu_k, *, num_qo_heads: int, num_kv_heads: int, head_dim: int,
+                    causal: bool = True, window_left: int = -1, sm_scale: float | None = None, lib=None):
+    """Dense varlen attention over contiguous per-segment K/V runs (DenseAttentionManager).
+    q_bits [Tq, Hq, D], k_bits / v_bits [Tk, Hkv, D] uint16; returns (out, lse) float32."""
+    lib = lib or load()
+    q, k, v = _u16(q_bits), _u16(k_bits), _u16(v_bits)
+    cq, ck = _i32(cu_q), _i32(cu_k)
+    if sm_scale is None:
+        sm_scale = 1.0 / float(np.sqrt(head_dim))
+    T = int(cq[-1])
+    out = np.full((T, num_qo_heads, head_dim), np.nan, dtype=np.float32)
+    lse = np.full((T, num_qo_heads), np.nan, dtype=np.float32)
+    rc = lib.oracle_dense_attention(_ptr(q), _ptr(k), _ptr(v), _ptr(cq), _ptr(ck), len(cq) - 1, num_qo_heads,
+                                    num_kv_heads, head_dim, int(bool(causal)), int(window_left), float(sm_scale),
+                                    _ptr(out), _ptr(lse))
+    if rc != 0:
+        raise ValueError(f"oracle_dense_attention rejected its input (code {rc})")
+    return out, lse

@@ -192,3 +192,62 @@ int oracle_kv_append(uint16_t *kv_layer, int64_t max_pages,
     }
     return 0;
 }
+
+/*
+ * Dense varlen attention (mstar.engine.resources.attn.dense, DenseAttentionManager /
+ * DensePlan): segment r attends over a contiguous K/V run, rows cu_k[r] .. cu_k[r+1] of
+ * k and v ([frozen prefix | fresh tokens], [total_k, num_kv_heads, head_dim] bf16 bits),
+ * with its queries q[cu_q[r] .. cu_q[r+1]) being the run's last n_r tokens: query i sits
+ * at position p = L_r - n_r + i, L_r = cu_k[r+1] - cu_k[r].  Visibility and arithmetic
+ * as in oracle_attention (causal 1 / non-causal 0, window_left).
+ */
+int oracle_dense_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                           const int32_t *cu_q, const int32_t *cu_k, int batch,
+                           int num_qo_heads, int num_kv_heads, int head_dim,
+                           int causal, int window_left, float sm_scale,
+                           float *out, float *lse)
+{
+    int group = num_qo_heads / num_kv_heads;
+    for (int r = 0; r < batch; ++r) {
+        int L = cu_k[r + 1] - cu_k[r];
+        int n = cu_q[r + 1] - cu_q[r];
+        if (n == 0) continue;
+        if (L < n) return -1;
+        float *s = (float *)malloc((size_t)L * sizeof(float));
+        if (!s) return -3;
+        for (int i = 0; i < n; ++i) {
+            int t = cu_q[r] + i;
+            int p = L - n + i;
+            int hi = causal ? p : L - 1;
+            int lo = 0;
+            if (window_left >= 0) lo = p - window_left > 0 ? p - window_left : 0;
+            for (int h = 0; h < num_qo_heads; ++h) {
+                int hk = h / group;
+                const uint16_t *qv = q + ((size_t)t * num_qo_heads + h) * head_dim;
+                float *o = out + ((size_t)t * num_qo_heads + h) * head_dim;
+                float m = -INFINITY;
+                for (int j = lo; j <= hi; ++j) {
+                    const uint16_t *kj = k + ((size_t)(cu_k[r] + j) * num_kv_heads + hk) * head_dim;
+                    float dot = 0.0f;
+                    for (int d = 0; d < head_dim; ++d) dot += bf16_bits_to_float(qv[d]) * bf16_bits_to_float(kj[d]);
+                    s[j] = sm_scale * dot;
+                    if (s[j] > m) m = s[j];
+                }
+                float l = 0.0f;
+                for (int j = lo; j <= hi; ++j) {
+                    s[j] = expf(s[j] - m);
+                    l += s[j];
+                }
+                for (int d = 0; d < head_dim; ++d) o[d] = 0.0f;
+                for (int j = lo; j <= hi; ++j) {
+                    const uint16_t *vj = v + ((size_t)(cu_k[r] + j) * num_kv_heads + hk) * head_dim;
+                    float w = s[j] / l;
+                    for (int d = 0; d < head_dim; ++d) o[d] += w * bf16_bits_to_float(vj[d]);
+                }
+                if (lse) lse[(size_t)t * num_qo_heads + h] = m + logf(l);
+            }
+        }
+        free(s);
+    }
+    return 0;
+}

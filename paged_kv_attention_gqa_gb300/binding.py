@@ -16,14 +16,15 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libpkv.so")
 
 OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_TOO_MANY_PREFILL_ROWS, ERR_NOT_PLANNED, ERR_CUDA, ERR_DEVICE = range(8)
-MODE_DECODE, MODE_PREFILL, MODE_MIXED = 0, 1, 2
+MODE_DECODE, MODE_PREFILL, MODE_MIXED, MODE_DENSE = 0, 1, 2, 3
 NON_CAUSAL, CAUSAL, CONTEXT_ONLY = 0, 1, 2
 STATUS_NAMES = ["OK", "INVALID", "UNSUPPORTED", "WORKSPACE", "TOO_MANY_PREFILL_ROWS", "NOT_PLANNED", "CUDA", "DEVICE"]
 
 # every symbol include/pkv.h declares
 EXPORTS = ["pkv_create", "pkv_destroy", "pkv_last_error", "pkv_workspace_size", "pkv_plan", "pkv_kv_append",
            "pkv_run_decode", "pkv_run_prefill", "pkv_run_mixed", "pkv_check_device_error", "pkv_append_slots",
-           "pkv_mixed_layout", "pkv_decode_split", "pkv_run_decode_static", "pkv_context_only_views"]
+           "pkv_mixed_layout", "pkv_decode_split", "pkv_run_decode_static", "pkv_context_only_views",
+           "pkv_plan_dense", "pkv_run_dense", "pkv_gather_kv"]
 
 
 class PkvError(RuntimeError):
@@ -67,6 +68,9 @@ def load(path: str = LIB_PATH):
         "pkv_decode_split": ([vp, i32p, i32p, i, i, i32p, ctypes.POINTER(i), ctypes.POINTER(i)], i),
         "pkv_run_decode_static": ([vp, vp, vp, vp, vp, i32p, i32p, i32p, i, i, ctypes.c_float, vp], i),
         "pkv_context_only_views": ([i, i32p, i32p, i32p, i32p, i, i32p, i32p, i32p, ctypes.POINTER(i)], i),
+        "pkv_plan_dense": ([vp, i32p, i32p, i, i, i, ctypes.c_float, vp, ctypes.c_size_t, vp], i),
+        "pkv_run_dense": ([vp, vp, vp, vp, vp, vp, vp, vp], i),
+        "pkv_gather_kv": ([vp, vp, vp, i, vp, vp, vp], i),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -161,6 +165,21 @@ class Handle:
 
     def run_mixed(self, q, kv_layer, out, lse=None, *, workspace, stream=None):
         self._run(self.lib.pkv_run_mixed, q, kv_layer, out, lse, workspace, stream)
+
+    def plan_dense(self, cu_q, cu_k, *, workspace, causal=True, window_left=-1, sm_scale=0.0, stream=None):
+        cq, ck = _i32(cu_q), _i32(cu_k)
+        self._check(self.lib.pkv_plan_dense(self.h, _p(cq), _p(ck), len(cq) - 1, int(bool(causal)), int(window_left),
+                                            float(sm_scale), _dptr(workspace),
+                                            workspace.numel() * workspace.element_size(), _stream(stream)))
+
+    def run_dense(self, q, k, v, out, lse=None, *, workspace, stream=None):
+        self._check(self.lib.pkv_run_dense(self.h, _dptr(q), _dptr(k), _dptr(v), _dptr(out), _dptr(lse),
+                                           _dptr(workspace), _stream(stream)))
+
+    def gather_kv(self, kv_layer, pages, num_tokens, k_out, v_out, stream=None):
+        """pages: a device int32 tensor of page ids."""
+        self._check(self.lib.pkv_gather_kv(self.h, _dptr(kv_layer), _dptr(pages), int(num_tokens), _dptr(k_out),
+                                           _dptr(v_out), _stream(stream)))
 
     def check_device_error(self, workspace, stream=None) -> int:
         code = ctypes.c_int()

@@ -343,10 +343,39 @@ __global__ void __launch_bounds__(256) append_kernel(const PlanHeader *hdr, cons
     }
 }
 
+// Gather of a frozen prefix (DenseAttentionManager): one warp per position t copies
+// K and V of slot t % page_size of page pages[t / page_size] to row t of k_out / v_out.
+__global__ void __launch_bounds__(256) gather_kernel(const uint4 *cache, const int32_t *pages, int num_tokens,
+                                                     int vec_per_token, int page_size, uint4 *k_out, uint4 *v_out) {
+    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t >= num_tokens) return;
+    const size_t row = (size_t)pages[t / page_size] * 2 * page_size + t % page_size;
+    const int lane = threadIdx.x & 31;
+    const uint4 *ks = cache + row * vec_per_token;
+    const uint4 *vs = cache + (row + page_size) * vec_per_token;
+    uint4 *kd = k_out + (size_t)t * vec_per_token;
+    uint4 *vd = v_out + (size_t)t * vec_per_token;
+    for (int i = lane; i < vec_per_token; i += 32) {
+        kd[i] = ks[i];
+        vd[i] = vs[i];
+    }
+}
+
 }  // namespace dev
 
 // ------------------------------------------------------------------------------------
 // launchers
+
+cudaError_t launch_gather(const Shape &s, const void *kv_layer, const int32_t *pages, int num_tokens, void *k_out,
+                          void *v_out, cudaStream_t st) {
+    if (num_tokens <= 0) return cudaSuccess;
+    const int vec = s.num_kv_heads * s.head_dim * 2 / 16;
+    const int wpb = 8;
+    dev::gather_kernel<<<(num_tokens + wpb - 1) / wpb, wpb * 32, 0, st>>>(
+        static_cast<const uint4 *>(kv_layer), pages, num_tokens, vec, s.page_size, static_cast<uint4 *>(k_out),
+        static_cast<uint4 *>(v_out));
+    return cudaGetLastError();
+}
 
 static uint32_t decode_stage_bytes(const Shape &s) {
     return 2u * (uint32_t)s.page_size * s.num_kv_heads * s.head_dim * 2u;

@@ -102,27 +102,15 @@ extern "C" const char *pkv_last_error(pkv_handle_t h) { return h ? h->err.c_str(
 
 extern "C" pkv_status pkv_workspace_size(pkv_handle_t h, int mode, size_t *bytes) {
     if (!h || !bytes) return fail(h, PKV_ERR_INVALID, "null argument");
-    if (mode < PKV_MODE_DECODE || mode > PKV_MODE_MIXED) return fail(h, PKV_ERR_INVALID, "unknown mode");
+    if (mode < PKV_MODE_DECODE || mode > PKV_MODE_DENSE) return fail(h, PKV_ERR_INVALID, "unknown mode");
     *bytes = pkv::workspace_bound(h->shape, mode);
     return PKV_OK;
 }
 
-extern "C" pkv_status pkv_plan(pkv_handle_t h, int mode, const int32_t *qo_indptr, const int32_t *kv_indptr,
-                               const int32_t *kv_indices, const int32_t *last_page_len, int batch, int causal,
-                               int window_left, float sm_scale, void *workspace, size_t workspace_bytes,
-                               pkv_stream_t stream) {
-    if (!h) return fail(h, PKV_ERR_INVALID, "null handle");
-    if (!workspace) return fail(h, PKV_ERR_INVALID, "null workspace");
-    if (reinterpret_cast<uintptr_t>(workspace) % pkv::kAlign)
-        return fail(h, PKV_ERR_INVALID, "workspace must be 256-byte aligned");
-    if (!(sm_scale >= 0.f) || std::isinf(sm_scale)) return fail(h, PKV_ERR_INVALID, "sm_scale must be finite and >= 0");
-    if (mode == PKV_MODE_MIXED && h->shape.max_prefill_rows < 0) return fail(h, PKV_ERR_INVALID, "no mixed config");
-    std::string err;
-    Plan plan;
-    int rc = pkv::make_plan(h->shape, mode, qo_indptr, kv_indptr, kv_indices, last_page_len, batch, causal,
-                            window_left, sm_scale, plan, err);
-    h->planned_ws = nullptr;
-    if (rc) return fail(h, (pkv_status)rc, err);
+// Copy a plan's integer image into the workspace through the page-locked ring (one
+// async H2D) and make it the handle's current plan.
+static pkv_status stage_plan(pkv_handle_t h, Plan &plan, void *workspace, size_t workspace_bytes,
+                             pkv_stream_t stream) {
     if (plan.lay.total > workspace_bytes)
         return fail(h, PKV_ERR_WORKSPACE,
                     "workspace of " + std::to_string(workspace_bytes) + " bytes is too small: this plan needs " +
@@ -162,6 +150,26 @@ extern "C" pkv_status pkv_plan(pkv_handle_t h, int mode, const int32_t *qo_indpt
     return PKV_OK;
 }
 
+
+extern "C" pkv_status pkv_plan(pkv_handle_t h, int mode, const int32_t *qo_indptr, const int32_t *kv_indptr,
+                               const int32_t *kv_indices, const int32_t *last_page_len, int batch, int causal,
+                               int window_left, float sm_scale, void *workspace, size_t workspace_bytes,
+                               pkv_stream_t stream) {
+    if (!h) return fail(h, PKV_ERR_INVALID, "null handle");
+    if (!workspace) return fail(h, PKV_ERR_INVALID, "null workspace");
+    if (reinterpret_cast<uintptr_t>(workspace) % pkv::kAlign)
+        return fail(h, PKV_ERR_INVALID, "workspace must be 256-byte aligned");
+    if (!(sm_scale >= 0.f) || std::isinf(sm_scale)) return fail(h, PKV_ERR_INVALID, "sm_scale must be finite and >= 0");
+    if (mode == PKV_MODE_MIXED && h->shape.max_prefill_rows < 0) return fail(h, PKV_ERR_INVALID, "no mixed config");
+    std::string err;
+    Plan plan;
+    int rc = pkv::make_plan(h->shape, mode, qo_indptr, kv_indptr, kv_indices, last_page_len, batch, causal,
+                            window_left, sm_scale, plan, err);
+    h->planned_ws = nullptr;
+    if (rc) return fail(h, (pkv_status)rc, err);
+    return stage_plan(h, plan, workspace, workspace_bytes, stream);
+}
+
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -179,15 +187,24 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // Tensor map over one layer slice viewed as [Hkv][pages * 2 * page_size rows][D] with the
 // head dimension OUTERMOST, so that a box of (64 columns, page_size slots, heads) lands
 // in shared memory head-major: each head's slots are consecutive 128-byte rows.
+static pkv_status encode_rows(pkv_handle_t h, const void *base, long long rows, int box_heads, CUtensorMap *tm);
+
 static pkv_status encode_kv(pkv_handle_t h, const void *kv_layer, int box_heads, CUtensorMap *tm) {
+    return encode_rows(h, kv_layer, (long long)h->shape.num_cache_pages * 2 * h->shape.page_size, box_heads, tm);
+}
+
+// Tensor map over [rows][Hkv][D] bf16 rows of Hkv*D elements (a layer slice viewed as
+// pages*2*page_size rows, or a contiguous K or V tensor), boxes of (64 columns, 16 rows,
+// box_heads heads), heads outermost so that one head's rows land contiguously.
+static pkv_status encode_rows(pkv_handle_t h, const void *kv_layer, long long rows, int box_heads, CUtensorMap *tm) {
     auto fn = encode_fn();
     if (!fn) return fail(h, PKV_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
     const Shape &s = h->shape;
     if (reinterpret_cast<uintptr_t>(kv_layer) % 16) return fail(h, PKV_ERR_INVALID, "kv_layer must be 16-byte aligned");
-    cuuint64_t dims[3] = {(cuuint64_t)s.head_dim, (cuuint64_t)s.num_cache_pages * 2 * s.page_size,
-                          (cuuint64_t)s.num_kv_heads};
+    cuuint64_t dims[3] = {(cuuint64_t)s.head_dim, (cuuint64_t)rows, (cuuint64_t)s.num_kv_heads};
     cuuint64_t strides[2] = {(cuuint64_t)s.num_kv_heads * s.head_dim * 2, (cuuint64_t)s.head_dim * 2};
     cuuint32_t box[3] = {64, (cuuint32_t)s.page_size, (cuuint32_t)box_heads};
+    if (rows < 1) return fail(h, PKV_ERR_INVALID, "a K / V tensor needs at least one row");
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(kv_layer), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -285,7 +302,7 @@ extern "C" pkv_status pkv_run_prefill(pkv_handle_t h, const void *q, const void 
     if ((st = check_io(h, q, kv_layer, out)) != PKV_OK) return st;
     if ((st = pf_map(h, kv_layer)) != PKV_OK) return st;
     if ((st = q_map(h, q, q_rows(h))) != PKV_OK) return st;
-    cudaError_t e = pkv::launch_prefill(h->shape, h->plan, h->tm_pf, h->tm_q, workspace, out, lse,
+    cudaError_t e = pkv::launch_prefill(h->shape, h->plan, h->tm_pf, h->tm_pf, h->tm_q, workspace, out, lse,
                                         static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PKV_OK : cuda_fail(h, e, "prefill launch");
 }
@@ -302,7 +319,7 @@ extern "C" pkv_status pkv_run_mixed(pkv_handle_t h, const void *q, const void *k
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = pkv::launch_decode(h->shape, h->plan, h->tm_dec, workspace, q, out, lse, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "mixed decode-pass launch");
-    e = pkv::launch_prefill(h->shape, h->plan, h->tm_pf, h->tm_q, workspace, out, lse, s);
+    e = pkv::launch_prefill(h->shape, h->plan, h->tm_pf, h->tm_pf, h->tm_q, workspace, out, lse, s);
     return e == cudaSuccess ? PKV_OK : cuda_fail(h, e, "mixed prefill-pass launch");
 }
 
@@ -428,4 +445,53 @@ extern "C" pkv_status pkv_run_decode_static(pkv_handle_t h, const void *q, const
     if (e != cudaSuccess) return cuda_fail(h, e, "static plan H2D");
     e = pkv::launch_decode(h->shape, plan, h->tm_dec, scratch, q, out, lse, s);
     return e == cudaSuccess ? PKV_OK : cuda_fail(h, e, "static decode launch");
+}
+
+// ---------------- dense varlen attention ----------------
+
+extern "C" pkv_status pkv_plan_dense(pkv_handle_t h, const int32_t *cu_q, const int32_t *cu_k, int batch, int causal,
+                                     int window_left, float sm_scale, void *workspace, size_t workspace_bytes,
+                                     pkv_stream_t stream) {
+    if (!h) return fail(h, PKV_ERR_INVALID, "null handle");
+    if (!workspace) return fail(h, PKV_ERR_INVALID, "null workspace");
+    if (reinterpret_cast<uintptr_t>(workspace) % pkv::kAlign)
+        return fail(h, PKV_ERR_INVALID, "workspace must be 256-byte aligned");
+    if (!(sm_scale >= 0.f) || std::isinf(sm_scale)) return fail(h, PKV_ERR_INVALID, "sm_scale must be finite and >= 0");
+    std::string err;
+    Plan plan;
+    int rc = pkv::make_dense_plan(h->shape, cu_q, cu_k, batch, causal, window_left, sm_scale, plan, err);
+    h->planned_ws = nullptr;
+    if (rc) return fail(h, (pkv_status)rc, err);
+    return stage_plan(h, plan, workspace, workspace_bytes, stream);
+}
+
+extern "C" pkv_status pkv_run_dense(pkv_handle_t h, const void *q, const void *k, const void *v, void *out, float *lse,
+                                    void *workspace, pkv_stream_t stream) {
+    pkv_status st = check_planned(h, workspace, PKV_MODE_DENSE);
+    if (st != PKV_OK) return st;
+    if (h->plan.num_tokens == 0) return PKV_OK;
+    if ((st = check_io(h, q, k, out)) != PKV_OK) return st;
+    if (!v || (reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) % 16)
+        return fail(h, PKV_ERR_INVALID, "k and v must be non-null and 16-byte aligned");
+    CUtensorMap tk, tv;
+    if ((st = encode_rows(h, k, h->plan.num_keys, 1, &tk)) != PKV_OK) return st;
+    if ((st = encode_rows(h, v, h->plan.num_keys, 1, &tv)) != PKV_OK) return st;
+    if ((st = q_map(h, q, h->plan.num_tokens)) != PKV_OK) return st;
+    cudaError_t e = pkv::launch_prefill(h->shape, h->plan, tk, tv, h->tm_q, workspace, out, lse,
+                                        static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : cuda_fail(h, e, "dense launch");
+}
+
+extern "C" pkv_status pkv_gather_kv(pkv_handle_t h, const void *kv_layer, const int32_t *pages, int num_tokens,
+                                    void *k_out, void *v_out, pkv_stream_t stream) {
+    if (!h) return fail(h, PKV_ERR_INVALID, "null handle");
+    if (num_tokens < 0) return fail(h, PKV_ERR_INVALID, "num_tokens must be >= 0");
+    if (num_tokens == 0) return PKV_OK;
+    if (!kv_layer || !pages || !k_out || !v_out) return fail(h, PKV_ERR_INVALID, "null argument");
+    if ((reinterpret_cast<uintptr_t>(kv_layer) | reinterpret_cast<uintptr_t>(k_out) |
+         reinterpret_cast<uintptr_t>(v_out)) % 16)
+        return fail(h, PKV_ERR_INVALID, "kv_layer, k_out and v_out must be 16-byte aligned");
+    cudaError_t e = pkv::launch_gather(h->shape, kv_layer, pages, num_tokens, k_out, v_out,
+                                       static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : cuda_fail(h, e, "gather launch");
 }

@@ -34,6 +34,7 @@ struct PlanHeader {
     int32_t causal;
     int32_t window_left;
     float scale_log2;     // sm_scale * log2(e)
+    int32_t dense;        // prefill tiles read contiguous K / V runs instead of pages
 };
 static_assert(sizeof(PlanHeader) <= kAlign, "the header fits its aligned slot");
 
@@ -111,6 +112,7 @@ struct Plan {
     int mode = -1;
     int batch = 0;
     int num_tokens = 0;          // T (decode: batch)
+    int num_keys = 0;            // dense plans: rows of the contiguous K / V
     int causal = 1;
     int window_left = -1;
     float sm_scale = 0.f;
@@ -146,6 +148,10 @@ void decode_split(const Shape &s, int rows, const int32_t *kvp, const int32_t *l
                   const int32_t *out_token, int window_left, std::vector<DecodeTile> &tiles,
                   std::vector<int32_t> &cta_ptr, std::vector<MergeRow> &merges, int &num_partials);
 int decode_cta_limit(const Shape &s);
+// Dense varlen plan (mstar.engine.resources.attn.dense, DensePlan): segment r's queries are
+// q[cu_q[r]..cu_q[r+1]), its keys rows cu_k[r]..cu_k[r+1] of contiguous K / V.
+int make_dense_plan(const Shape &s, const int32_t *cu_q, const int32_t *cu_k, int batch, int causal, int window_left,
+                    float sm_scale, Plan &plan, std::string &err);
 int make_plan(const Shape &s, int mode, const int32_t *qo, const int32_t *kvp, const int32_t *kvi,
               const int32_t *lpl, int batch, int causal, int window_left, float sm_scale, Plan &plan,
               std::string &err);

@@ -277,18 +277,22 @@ void decode_split(const Shape &s, int rows, const int32_t *kvp, const int32_t *l
     }
 }
 
-static void prefill_tiles(const Shape &s, const std::vector<int> &rows, const int32_t *q_begin_of_row,
-                          const int32_t *qo, const int32_t *kvp, const int32_t *lpl, int causal, int window_left,
-                          std::vector<PrefillTile> &out) {
-    const int P = s.page_size;
+struct PrefillRow {
+    int n;        // queries
+    int L;        // keys
+    int q_begin;  // first query token in q / out
+    int kv_base;  // paged: offset of the first page in the page list; dense: first key row
+};
+
+static void prefill_tiles_rows(const Shape &s, const std::vector<PrefillRow> &rows, int causal, int window_left,
+                               std::vector<PrefillTile> &out) {
     const int g = s.group();
     const int BQ = kPrefillRowsPerTile / g;
-    for (int r : rows) {
-        int n = qo[r + 1] - qo[r];
+    for (const PrefillRow &pr : rows) {
+        const int n = pr.n, L = pr.L;
         if (n <= 0) continue;
-        int L = row_len(kvp, lpl, r, P);
         // causal 2 (context-only): the row's pages hold the context; its queries follow it
-        int c = causal == 2 ? L : L - n;
+        const int c = causal == 2 ? L : L - n;
         for (int t0 = 0; t0 < n; t0 += BQ) {
             int nq = std::min(BQ, n - t0);
             int p0 = c + t0, p1 = c + t0 + nq - 1;
@@ -297,11 +301,11 @@ static void prefill_tiles(const Shape &s, const std::vector<int> &rows, const in
             if (ke <= kb) kb = ke = 0;  // no query of the tile sees a key: zeros, lse -inf
             for (int hk = 0; hk < s.num_kv_heads; ++hk) {
                 PrefillTile t;
-                t.q_begin = q_begin_of_row[r] + t0;
+                t.q_begin = pr.q_begin + t0;
                 t.n_q = nq;
                 t.pos0 = p0;
                 t.length = L;
-                t.kv_base = kvp[r];
+                t.kv_base = pr.kv_base;
                 t.kv_head = hk;
                 t.key_begin = kb;
                 t.key_end = ke;
@@ -313,6 +317,15 @@ static void prefill_tiles(const Shape &s, const std::vector<int> &rows, const in
     std::stable_sort(out.begin(), out.end(), [](const PrefillTile &a, const PrefillTile &b) {
         return (a.key_end - a.key_begin) > (b.key_end - b.key_begin);
     });
+}
+
+static void prefill_tiles(const Shape &s, const std::vector<int> &rows, const int32_t *q_begin_of_row,
+                          const int32_t *qo, const int32_t *kvp, const int32_t *lpl, int causal, int window_left,
+                          std::vector<PrefillTile> &out) {
+    std::vector<PrefillRow> prs;
+    for (int r : rows)
+        prs.push_back(PrefillRow{qo[r + 1] - qo[r], row_len(kvp, lpl, r, s.page_size), q_begin_of_row[r], kvp[r]});
+    prefill_tiles_rows(s, prs, causal, window_left, out);
 }
 
 static int prefill_tile_bound(const Shape &s, int rows, int tokens) {
@@ -353,6 +366,12 @@ StaticCounts static_counts(const Shape &s, int mode) {
     StaticCounts c;
     const int C = decode_cta_limit(s);
     const int rows = s.max_batch;
+    if (mode == PKV_MODE_DENSE) {
+        c.tokens = s.max_total_tokens;
+        c.dec_nnz = c.pf_nnz = c.dec_tiles = c.dec_ctas = c.num_merge = c.partials = 0;
+        c.pf_tiles = prefill_tile_bound(s, rows, c.tokens);
+        return c;
+    }
     const int dec_rows = mode == PKV_MODE_PREFILL ? 0 : rows;
     c.tokens = mode == PKV_MODE_DECODE ? s.max_batch : s.max_total_tokens;
     c.dec_nnz = mode == PKV_MODE_DECODE ? s.max_num_pages : (mode == PKV_MODE_MIXED ? s.max_num_pages + rows : 0);
@@ -375,6 +394,54 @@ size_t workspace_bound(const Shape &s, int mode) {
 template <class T>
 static void put(std::vector<uint8_t> &img, size_t off, const T *src, size_t n) {
     if (n) std::memcpy(img.data() + off, src, n * sizeof(T));
+}
+
+// Layout, device header and workspace image of a plan whose pieces are built.
+static void finish_plan(const Shape &s, Plan &plan, int T, int window_left, const std::vector<int32_t> &app,
+                        const std::vector<int32_t> &dec_pages, const std::vector<int32_t> &pf_pages,
+                        const std::vector<DecodeTile> &dtiles, std::vector<int32_t> &cta_ptr,
+                        const std::vector<MergeRow> &merges, const std::vector<PrefillTile> &ptiles, int partials) {
+    const int mode = plan.mode;
+    plan.dec_nnz = (int)dec_pages.size();
+    plan.pf_nnz = (int)pf_pages.size();
+    plan.dec_tiles = (int)dtiles.size();
+    plan.dec_ctas = dtiles.empty() ? 0 : (int)cta_ptr.size() - 1;
+    plan.num_merge = (int)merges.size();
+    plan.num_partials = partials;
+    plan.pf_tiles = (int)ptiles.size();
+    if (s.graph_static) {
+        // fixed layout at the maxima: captured launches keep pointing at the right arrays;
+        // idle decode CTAs get empty tile ranges
+        const StaticCounts c = static_counts(s, mode);
+        plan.lay = layout_for(s, c.tokens, c.dec_nnz, c.pf_nnz, c.dec_tiles, c.dec_ctas, c.num_merge, c.pf_tiles,
+                              c.partials);
+        if (c.dec_ctas) {
+            if (cta_ptr.empty()) cta_ptr.assign(1, 0);
+            while ((int)cta_ptr.size() < c.dec_ctas + 1) cta_ptr.push_back(cta_ptr.back());
+        }
+    } else {
+        plan.lay = layout_for(s, T, plan.dec_nnz, plan.pf_nnz, plan.dec_tiles, plan.dec_ctas, plan.num_merge,
+                              plan.pf_tiles, partials);
+    }
+    plan.image.assign(plan.lay.int_bytes, 0);
+    PlanHeader hdr;
+    hdr.err = 0;
+    hdr.num_append = plan.num_append;
+    hdr.dec_ctas = plan.dec_ctas;
+    hdr.num_merge = plan.num_merge;
+    hdr.pf_tiles = plan.pf_tiles;
+    hdr.causal = plan.causal;
+    hdr.window_left = window_left;
+    hdr.scale_log2 = plan.sm_scale * 1.4426950408889634f;
+    hdr.dense = mode == PKV_MODE_DENSE ? 1 : 0;
+    put(plan.image, plan.lay.err, &hdr, 1);
+    put(plan.image, plan.lay.append_rows, app.data(), app.size());
+    put(plan.image, plan.lay.dec_pages, dec_pages.data(), dec_pages.size());
+    put(plan.image, plan.lay.pf_pages, pf_pages.data(), pf_pages.size());
+    put(plan.image, plan.lay.dec_tiles, dtiles.data(), dtiles.size());
+    if (!cta_ptr.empty() && (plan.dec_ctas || s.graph_static)) put(plan.image, plan.lay.dec_cta_ptr, cta_ptr.data(), cta_ptr.size());
+    put(plan.image, plan.lay.merge_rows, merges.data(), merges.size());
+    put(plan.image, plan.lay.pf_tiles, ptiles.data(), ptiles.size());
 }
 
 int make_plan(const Shape &s, int mode, const int32_t *qo, const int32_t *kvp, const int32_t *kvi,
@@ -453,45 +520,57 @@ int make_plan(const Shape &s, int mode, const int32_t *qo, const int32_t *kvp, c
         err = "unknown plan mode";
         return PKV_ERR_INVALID;
     }
-    plan.dec_nnz = (int)dec_pages.size();
-    plan.pf_nnz = (int)pf_pages.size();
-    plan.dec_tiles = (int)dtiles.size();
-    plan.dec_ctas = dtiles.empty() ? 0 : (int)cta_ptr.size() - 1;
-    plan.num_merge = (int)merges.size();
-    plan.num_partials = partials;
-    plan.pf_tiles = (int)ptiles.size();
-    if (s.graph_static) {
-        // fixed layout at the maxima: captured launches keep pointing at the right arrays;
-        // idle decode CTAs get empty tile ranges
-        const StaticCounts c = static_counts(s, mode);
-        plan.lay = layout_for(s, c.tokens, c.dec_nnz, c.pf_nnz, c.dec_tiles, c.dec_ctas, c.num_merge, c.pf_tiles,
-                              c.partials);
-        if (c.dec_ctas) {
-            if (cta_ptr.empty()) cta_ptr.assign(1, 0);
-            while ((int)cta_ptr.size() < c.dec_ctas + 1) cta_ptr.push_back(cta_ptr.back());
-        }
-    } else {
-        plan.lay = layout_for(s, T, plan.dec_nnz, plan.pf_nnz, plan.dec_tiles, plan.dec_ctas, plan.num_merge,
-                              plan.pf_tiles, partials);
+    finish_plan(s, plan, T, window_left, app, dec_pages, pf_pages, dtiles, cta_ptr, merges, ptiles, partials);
+    return PKV_OK;
+}
+
+int make_dense_plan(const Shape &s, const int32_t *cu_q, const int32_t *cu_k, int batch, int causal, int window_left,
+                    float sm_scale, Plan &plan, std::string &err) {
+    if (!cu_q || !cu_k || batch < 0 || batch > s.max_batch) {
+        err = "cu_q and cu_k are required and batch must be in [0, max_batch]";
+        return PKV_ERR_INVALID;
     }
-    plan.image.assign(plan.lay.int_bytes, 0);
-    PlanHeader hdr;
-    hdr.err = 0;
-    hdr.num_append = plan.num_append;
-    hdr.dec_ctas = plan.dec_ctas;
-    hdr.num_merge = plan.num_merge;
-    hdr.pf_tiles = plan.pf_tiles;
-    hdr.causal = plan.causal;
-    hdr.window_left = window_left;
-    hdr.scale_log2 = plan.sm_scale * 1.4426950408889634f;
-    put(plan.image, plan.lay.err, &hdr, 1);
-    put(plan.image, plan.lay.append_rows, app.data(), app.size());
-    put(plan.image, plan.lay.dec_pages, dec_pages.data(), dec_pages.size());
-    put(plan.image, plan.lay.pf_pages, pf_pages.data(), pf_pages.size());
-    put(plan.image, plan.lay.dec_tiles, dtiles.data(), dtiles.size());
-    if (!cta_ptr.empty() && (plan.dec_ctas || s.graph_static)) put(plan.image, plan.lay.dec_cta_ptr, cta_ptr.data(), cta_ptr.size());
-    put(plan.image, plan.lay.merge_rows, merges.data(), merges.size());
-    put(plan.image, plan.lay.pf_tiles, ptiles.data(), ptiles.size());
+    if (causal != 0 && causal != 1) {
+        err = "dense plans are causal (1) or non-causal (0)";
+        return PKV_ERR_INVALID;
+    }
+    if (window_left < -1) {
+        err = "window_left must be -1 (unbounded) or >= 0";
+        return PKV_ERR_INVALID;
+    }
+    if (cu_q[0] != 0 || cu_k[0] != 0) {
+        err = "cu_q and cu_k must start at 0";
+        return PKV_ERR_INVALID;
+    }
+    std::vector<PrefillRow> rows;
+    for (int r = 0; r < batch; ++r) {
+        const int n = cu_q[r + 1] - cu_q[r], L = cu_k[r + 1] - cu_k[r];
+        if (n < 0 || L < 0) {
+            err = "cu_q / cu_k decrease at segment " + std::to_string(r);
+            return PKV_ERR_INVALID;
+        }
+        if (n > L) {
+            err = "segment " + std::to_string(r) + " has more queries than keys (its fresh tokens are part of its keys)";
+            return PKV_ERR_INVALID;
+        }
+        rows.push_back(PrefillRow{n, L, cu_q[r], cu_k[r]});
+    }
+    if (cu_q[batch] > s.max_total_tokens) {
+        err = "dense plan has " + std::to_string(cu_q[batch]) + " queries, above max_total_tokens";
+        return PKV_ERR_INVALID;
+    }
+    plan = Plan();
+    plan.mode = PKV_MODE_DENSE;
+    plan.batch = batch;
+    plan.causal = causal;
+    plan.window_left = window_left;
+    plan.sm_scale = sm_scale > 0.f ? sm_scale : 1.0f / std::sqrt((float)s.head_dim);
+    plan.num_tokens = cu_q[batch];
+    plan.num_keys = cu_k[batch];
+    std::vector<PrefillTile> ptiles;
+    prefill_tiles_rows(s, rows, causal, window_left, ptiles);
+    std::vector<int32_t> none, cta;
+    finish_plan(s, plan, plan.num_tokens, window_left, none, none, none, {}, cta, {}, ptiles, 0);
     return PKV_OK;
 }
 

@@ -65,8 +65,8 @@ struct PfSmem {
 
 template <int D, int G>
 __global__ void __launch_bounds__(kPfThreads, 2)
-    prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_q,
-                      const PrefillArgs a) {
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_v,
+                      const __grid_constant__ CUtensorMap tm_q, const PrefillArgs a) {
     using L = PfSmem<D>;
     constexpr int HALVES = L::HALVES;
     constexpr int BQ = kPrefillRowsPerTile / G;
@@ -94,6 +94,9 @@ __global__ void __launch_bounds__(kPfThreads, 2)
     int *const err = &a.hdr->err;
     const int causal = a.hdr->causal;
     const int window_left = a.hdr->window_left;
+    // dense varlen plans: K and V rows come from two contiguous tensors (tm_kv, tm_v),
+    // tile keys at rows kv_base + key; paged plans: both from the layer slice (tm_kv)
+    const bool dense = a.hdr->dense != 0;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int P = a.page_size;
@@ -130,6 +133,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
         // ------------------------------------------------ producer
         if (lane == 0) {
             prefetch_tmap(&tm_kv);
+            prefetch_tmap(&tm_v);
             prefetch_tmap(&tm_q);
             mbar_arrive_expect_tx(q_full, L::Q_BYTES);
 #pragma unroll
@@ -144,7 +148,10 @@ __global__ void __launch_bounds__(kPfThreads, 2)
 #pragma unroll
                 for (int pg = 0; pg < 4; ++pg) {
                     const int pi = (kt0 + j) * 4 + pg;
-                    rows[pg] = pi < npages ? a.pages[t.kv_base + pi] * 2 * P : -1;
+                    if (dense)
+                        rows[pg] = t.kv_base + pi * P;  // past the segment: masked keys, finite V
+                    else
+                        rows[pg] = pi < npages ? a.pages[t.kv_base + pi] * 2 * P : -1;
                 }
                 if (use > 0 && !mbar_wait(&k_empty[s], (use - 1) & 1, err, kErrWaitEmpty)) break;
                 uint8_t *kd = sm + L::K_OFF + s * L::KV_BYTES;
@@ -162,8 +169,8 @@ __global__ void __launch_bounds__(kPfThreads, 2)
                 for (int pg = 0; pg < 4; ++pg)
 #pragma unroll
                     for (int h = 0; h < HALVES; ++h)
-                        tma_load_3d(vd + h * (L::KV_BYTES / HALVES) + pg * 2048, &tm_kv, &v_full[s], h * 64,
-                                    rows[pg] >= 0 ? rows[pg] + P : a.oob_row, t.kv_head);
+                        tma_load_3d(vd + h * (L::KV_BYTES / HALVES) + pg * 2048, dense ? &tm_v : &tm_kv, &v_full[s],
+                                    h * 64, rows[pg] < 0 ? a.oob_row : rows[pg] + (dense ? 0 : P), t.kv_head);
             }
         }
     } else if (warp == 5) {
@@ -379,17 +386,17 @@ size_t prefill_smem_bytes(const Shape &s) {
 }
 
 template <int D, int G>
-static cudaError_t launch_prefill_t(const CUtensorMap &tkv, const CUtensorMap &tq, const dev::PrefillArgs &a,
-                                    int grid, size_t smem, cudaStream_t st) {
+static cudaError_t launch_prefill_t(const CUtensorMap &tkv, const CUtensorMap &tv, const CUtensorMap &tq,
+                                    const dev::PrefillArgs &a, int grid, size_t smem, cudaStream_t st) {
     auto fn = dev::prefill_tc_kernel<D, G>;
     cudaError_t e = set_smem_limit((const void *)fn, smem, st);
     if (e != cudaSuccess) return e;
-    fn<<<grid, dev::kPfThreads, smem, st>>>(tkv, tq, a);
+    fn<<<grid, dev::kPfThreads, smem, st>>>(tkv, tv, tq, a);
     return cudaGetLastError();
 }
 
-cudaError_t launch_prefill(const Shape &s, const Plan &p, const CUtensorMap &tm_kv, const CUtensorMap &tm_q, void *ws,
-                           void *out, float *lse, cudaStream_t st) {
+cudaError_t launch_prefill(const Shape &s, const Plan &p, const CUtensorMap &tm_kv, const CUtensorMap &tm_v,
+                           const CUtensorMap &tm_q, void *ws, void *out, float *lse, cudaStream_t st) {
     const int grid = s.graph_static ? static_counts(s, p.mode).pf_tiles : p.pf_tiles;
     if (grid == 0) return cudaSuccess;
     uint8_t *w = static_cast<uint8_t *>(ws);
@@ -401,12 +408,13 @@ cudaError_t launch_prefill(const Shape &s, const Plan &p, const CUtensorMap &tm_
     a.hdr = reinterpret_cast<PlanHeader *>(w + p.lay.err);
     a.num_qo_heads = s.num_qo_heads;
     a.page_size = s.page_size;
+    // a row coordinate past the tensor (TMA fills zeros); dense plans never use it
     a.oob_row = s.num_cache_pages * 2 * s.page_size;
     const size_t smem = prefill_smem_bytes(s);
     cudaError_t e = cudaErrorInvalidValue;
     const int g = s.group();
 #define PKV_PF(DD, GG) \
-    if (s.head_dim == DD && g == GG) e = launch_prefill_t<DD, GG>(tm_kv, tm_q, a, grid, smem, st);
+    if (s.head_dim == DD && g == GG) e = launch_prefill_t<DD, GG>(tm_kv, tm_v, tm_q, a, grid, smem, st);
     PKV_PF(64, 1) PKV_PF(64, 2) PKV_PF(64, 4) PKV_PF(64, 8) PKV_PF(64, 16)
     PKV_PF(128, 1) PKV_PF(128, 2) PKV_PF(128, 4) PKV_PF(128, 8) PKV_PF(128, 16)
 #undef PKV_PF

@@ -79,7 +79,8 @@ def compare(out, lse, ref_out, ref_lse, tokens=None, what=""):
     max_abs = float(d.max()) if d.size else 0.0
     rel = float(np.linalg.norm(o - ref_out) / max(np.linalg.norm(ref_out), 1e-30)) if d.size else 0.0
     both_empty = np.isneginf(l) & np.isneginf(ref_lse)  # queries that see no key: lse = -inf on both sides
-    dl = np.where(both_empty, 0.0, np.abs(l - ref_lse))
+    with np.errstate(invalid="ignore"):
+        dl = np.where(both_empty, 0.0, np.abs(l - ref_lse))
     lse_ok = bool(np.all(dl <= LSE_REL * np.maximum(1.0, np.where(both_empty, 1.0, np.abs(ref_lse)))))
     assert max_abs <= MAX_ABS and rel <= REL_L2, f"{what}: max_abs {max_abs:.3e} rel_l2 {rel:.3e}"
     assert lse_ok, f"{what}: lse max diff {float(dl.max()):.3e}"

@@ -312,5 +312,33 @@ def pin_sdpa_context_only(lib=None, tol=2e-5):
         assert not fin.any() or np.abs(lse[fin] - rl.numpy()[fin]).max() <= tol, k
 
 
+def dense_from_paged(pb, kv_layer):
+    """Contiguous per-row K/V runs ([prefix | new] = the row's L tokens) and cu arrays."""
+    ks, vs = [], []
+    for r in range(pb.batch):
+        K, V = wl.logical_kv(pb, kv_layer, r)
+        ks.append(K)
+        vs.append(V)
+    cu_k = np.concatenate([[0], np.cumsum(pb.kv_lens)]).astype(np.int32)
+    return torch.cat(ks), torch.cat(vs), pb.qo_indptr, cu_k
+
+
+def pin_dense(lib=None, tol=2e-5):
+    """Dense varlen over the rows' contiguous K/V equals the paged oracle on the same
+    logical K/V bit for bit (same definition, same order), and SDPA in float64."""
+    for k, (Ls, ns, Hq, Hkv, D, P, causal, wleft) in enumerate(SDPA_CASES[:5]):
+        pb = wl.custom(300 + k, Ls, ns, num_qo_heads=Hq, num_kv_heads=Hkv, head_dim=D, page_size=P)
+        q, kv, _ = build_step(pb, seed=k)
+        K, V, cu_q, cu_k = dense_from_paged(pb, kv)
+        d_o, d_l = oracle.dense_attention(wl.bf16_bits(q), wl.bf16_bits(K), wl.bf16_bits(V), cu_q, cu_k,
+                                          num_qo_heads=Hq, num_kv_heads=Hkv, head_dim=D, causal=causal,
+                                          window_left=wleft, sm_scale=0.3, lib=lib)
+        p_o, p_l = run_oracle(pb, q, kv, causal=causal, window_left=wleft, sm_scale=0.3, lib=lib)
+        assert np.array_equal(d_o, p_o) and np.array_equal(d_l, p_l), k
+        ro, rl = sdpa_reference(pb, q, kv, causal=causal, window_left=wleft, sm_scale=0.3)
+        assert np.abs(d_o - ro.numpy()).max() <= tol and np.abs(d_l - rl.numpy()).max() <= tol, k
+
+
 ALL_PINS = [pin_golden, pin_sdpa, pin_pool_permutation, pin_page_size_invariance, pin_rows_sum_to_one,
-            pin_single_key_cases, pin_decode_is_one_token_prefill, pin_append, pin_sdpa_context_only]
+            pin_single_key_cases, pin_decode_is_one_token_prefill, pin_append, pin_sdpa_context_only,
+            pin_dense]

@@ -274,3 +274,79 @@ def test_context_only_views_then_prefill_matches_full_rows_without_their_queries
     out, lse, _, _ = G.gpu_step(ctx, x, "prefill", causal=B.CONTEXT_ONLY, append=False)
     ref_o, ref_l = G.oracle_attn(ctx, wl.bf16_bits(q), wl.bf16_bits(kv), causal=2)
     G.compare(out, lse, ref_o, ref_l, what="context-only views")
+
+
+# ------------------------------------------------------------------ dense varlen (DenseAttentionManager)
+
+def _dense_inputs(seed, n, L, Hq, Hkv, D):
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    Tq, Tk = int(np.sum(n)), int(np.sum(L))
+    q = torch.randn(Tq, Hq, D, generator=g, device="cuda").to(torch.bfloat16)
+    k = torch.randn(Tk, Hkv, D, generator=g, device="cuda").to(torch.bfloat16)
+    v = torch.randn(Tk, Hkv, D, generator=g, device="cuda").to(torch.bfloat16)
+    cu_q = np.concatenate([[0], np.cumsum(n)]).astype(np.int32)
+    cu_k = np.concatenate([[0], np.cumsum(L)]).astype(np.int32)
+    return q, k, v, cu_q, cu_k
+
+
+def _dense_handle(Hq, Hkv, D, batch, tokens):
+    from paged_kv_attention_gqa_gb300 import binding as B
+    return B.Handle(num_qo_heads=Hq, num_kv_heads=Hkv, head_dim=D, page_size=16, max_batch=batch,
+                    max_total_tokens=tokens, max_num_pages=1, num_cache_pages=1)
+
+
+@pytest.mark.parametrize("D,Hq,Hkv", [(128, 32, 8), (64, 16, 2)])
+@pytest.mark.parametrize("causal,window", [(True, -1), (False, -1), (True, 33)])
+def test_dense_matches_oracle(D, Hq, Hkv, causal, window):
+    import oracle
+    from paged_kv_attention_gqa_gb300 import binding as B
+    n = [1, 40, 130, 7, 64]
+    L = [1, 300, 130, 90, 1000]
+    q, k, v, cu_q, cu_k = _dense_inputs(70, n, L, Hq, Hkv, D)
+    h = _dense_handle(Hq, Hkv, D, len(n), int(np.sum(n)))
+    ws = torch.empty(h.workspace_size(B.MODE_DENSE), dtype=torch.uint8, device="cuda")
+    h.plan_dense(cu_q, cu_k, workspace=ws, causal=causal, window_left=window)
+    out = torch.full_like(q, float("nan"))
+    lse = torch.full(q.shape[:2], float("nan"), dtype=torch.float32, device="cuda")
+    h.run_dense(q, k, v, out, lse, workspace=ws)
+    torch.cuda.synchronize()
+    assert h.check_device_error(ws) == 0
+    ro, rl = oracle.dense_attention(wl.bf16_bits(q), wl.bf16_bits(k), wl.bf16_bits(v), cu_q, cu_k, num_qo_heads=Hq,
+                                    num_kv_heads=Hkv, head_dim=D, causal=causal, window_left=window)
+    G.compare(out, lse, ro, rl, what="dense")
+
+
+def test_dense_over_gathered_prefix_is_bit_identical_to_paged_prefill():
+    """Gather each row's frozen prefix from the pages (bit-exact), append the fresh K/V
+    after it, run the dense pass: the result equals the paged prefill over the same
+    cache bit for bit (same kernel, same key order)."""
+    from paged_kv_attention_gqa_gb300 import binding as B
+    n = [20, 1, 130, 64]
+    c = [100, 0, 33, 900]
+    pb = wl.custom(71, np.add(n, c), n, num_qo_heads=32, num_kv_heads=8, head_dim=128, page_size=16)
+    x = wl.make_inputs(pb, device="cuda", seed=14, unused="nan", layers=1)
+    out_p, lse_p, h, ws = G.gpu_step(pb, x, "prefill")
+    kv = x["kv_cache"][0]
+    cu_k = np.concatenate([[0], np.cumsum(pb.kv_lens)]).astype(np.int32)
+    k = torch.empty(int(cu_k[-1]), 8, 128, dtype=torch.bfloat16, device="cuda")
+    v = torch.empty_like(k)
+    qo = pb.qo_indptr
+    for r in range(pb.batch):
+        pages = torch.as_tensor(pb.page_table[r], dtype=torch.int32, device="cuda")
+        h.gather_kv(kv, pages, c[r], k[cu_k[r]:], v[cu_k[r]:])
+        k[cu_k[r] + c[r]: cu_k[r + 1]] = x["k_new"][qo[r]: qo[r + 1]]
+        v[cu_k[r] + c[r]: cu_k[r + 1]] = x["v_new"][qo[r]: qo[r + 1]]
+    torch.cuda.synchronize()
+    for r in range(pb.batch):
+        K, V = wl.logical_kv(pb, kv, r)
+        assert torch.equal(k[cu_k[r]: cu_k[r + 1]].view(torch.int16), K.view(torch.int16))
+        assert torch.equal(v[cu_k[r]: cu_k[r + 1]].view(torch.int16), V.view(torch.int16))
+    hd = _dense_handle(32, 8, 128, pb.batch, pb.num_tokens)
+    wsd = torch.empty(hd.workspace_size(B.MODE_DENSE), dtype=torch.uint8, device="cuda")
+    hd.plan_dense(pb.qo_indptr, cu_k, workspace=wsd)
+    out_d = torch.full_like(out_p, float("nan"))
+    lse_d = torch.full_like(lse_p, float("nan"))
+    hd.run_dense(x["q"], k, v, out_d, lse_d, workspace=wsd)
+    torch.cuda.synchronize()
+    assert torch.equal(out_d.view(torch.int16), out_p.view(torch.int16))
+    assert torch.equal(lse_d, lse_p)

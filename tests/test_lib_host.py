@@ -217,3 +217,21 @@ def test_context_only_needs_prefill_mode(lib):
     h = _handle(num_cache_pages=100, max_num_pages=100)
     st, msg = _plan_status(h, B.MODE_DECODE, (None, [0, 1], [3], [4]), causal=2)
     assert st == B.ERR_INVALID and "context" in msg
+
+
+def _dense_status(h, cu_q, cu_k, causal=1):
+    cq, ck = (np.ascontiguousarray(np.asarray(a, np.int32)) for a in (cu_q, cu_k))
+    p = lambda a: a.ctypes.data_as(ctypes.c_void_p)
+    st = h.lib.pkv_plan_dense(h.h, p(cq), p(ck), len(cq) - 1, causal, -1, 0.0, ctypes.c_void_p(1 << 20), 1024, None)
+    return st, h.lib.pkv_last_error(h.h).decode()
+
+
+def test_dense_plan_validation(lib):
+    h = _handle(max_total_tokens=100, max_batch=4)
+    assert _dense_status(h, [0, 5], [0, 4])[0] == B.ERR_INVALID          # more queries than keys
+    assert _dense_status(h, [0, 3, 2], [0, 4, 9])[0] == B.ERR_INVALID    # decreasing cu_q
+    assert _dense_status(h, [0, 101], [0, 200])[0] == B.ERR_INVALID      # above max_total_tokens
+    assert _dense_status(h, [0, 3], [0, 4], causal=2)[0] == B.ERR_INVALID
+    st, msg = _dense_status(h, [0, 3, 5], [0, 40, 50])                   # valid: too small a workspace
+    assert st == B.ERR_WORKSPACE, msg
+    assert h.workspace_size(B.MODE_DENSE) > 0
