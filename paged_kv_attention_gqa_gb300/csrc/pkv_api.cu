@@ -28,6 +28,9 @@ struct pkv_handle_s {
     cudaEvent_t fence[2] = {nullptr, nullptr};
     bool fence_live[2] = {false, false};
     int ring_at = 0;
+    // side stream + fork/join events of the mixed step's concurrent passes
+    cudaStream_t side = nullptr;
+    cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
     // last encoded tensor maps (re-encoded when the layer pointer changes)
     const void *tm_dec_ptr = nullptr, *tm_pf_ptr = nullptr, *tm_q_ptr = nullptr;
     int tm_q_rows = -1;
@@ -95,6 +98,12 @@ extern "C" void pkv_destroy(pkv_handle_t h) {
         }
         if (h->pinned[i]) cudaFreeHost(h->pinned[i]);
     }
+    if (h->side) {
+        cudaStreamSynchronize(h->side);
+        cudaStreamDestroy(h->side);
+    }
+    if (h->ev_fork) cudaEventDestroy(h->ev_fork);
+    if (h->ev_join) cudaEventDestroy(h->ev_join);
     delete h;
 }
 
@@ -317,10 +326,26 @@ extern "C" pkv_status pkv_run_mixed(pkv_handle_t h, const void *q, const void *k
     if ((st = pf_map(h, kv_layer)) != PKV_OK) return st;
     if ((st = q_map(h, q, q_rows(h))) != PKV_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = pkv::launch_decode(h->shape, h->plan, h->tm_dec, workspace, q, out, lse, s);
+    // The two passes write disjoint tokens and only read the cache: the decode pass (HBM-
+    // bound, on the SMs the plan gave it) runs on `stream`, the prefill pass (tensor-bound)
+    // on a side stream forked from it and joined back.
+    cudaError_t e = cudaSuccess;
+    if (!h->side) {
+        e = cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming);
+        if (e != cudaSuccess) return cuda_fail(h, e, "side stream (make the first mixed run outside a capture)");
+    }
+    e = cudaEventRecord(h->ev_fork, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(h->side, h->ev_fork, 0);
+    if (e != cudaSuccess) return cuda_fail(h, e, "mixed fork");
+    e = pkv::launch_decode(h->shape, h->plan, h->tm_dec, workspace, q, out, lse, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "mixed decode-pass launch");
-    e = pkv::launch_prefill(h->shape, h->plan, h->tm_pf, h->tm_pf, h->tm_q, workspace, out, lse, s);
-    return e == cudaSuccess ? PKV_OK : cuda_fail(h, e, "mixed prefill-pass launch");
+    e = pkv::launch_prefill(h->shape, h->plan, h->tm_pf, h->tm_pf, h->tm_q, workspace, out, lse, h->side);
+    if (e != cudaSuccess) return cuda_fail(h, e, "mixed prefill-pass launch");
+    e = cudaEventRecord(h->ev_join, h->side);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, h->ev_join, 0);
+    return e == cudaSuccess ? PKV_OK : cuda_fail(h, e, "mixed join");
 }
 
 extern "C" pkv_status pkv_check_device_error(pkv_handle_t h, void *workspace, pkv_stream_t stream, int *code) {

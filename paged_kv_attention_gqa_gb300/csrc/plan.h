@@ -146,7 +146,8 @@ int mixed_layout(const int32_t *qo, const int32_t *kvp, const int32_t *kvi, cons
 // Split the visible pages of a decode pass into per-CTA tiles.
 void decode_split(const Shape &s, int rows, const int32_t *kvp, const int32_t *lpl, const int32_t *q_token,
                   const int32_t *out_token, int window_left, std::vector<DecodeTile> &tiles,
-                  std::vector<int32_t> &cta_ptr, std::vector<MergeRow> &merges, int &num_partials);
+                  std::vector<int32_t> &cta_ptr, std::vector<MergeRow> &merges, int &num_partials,
+                  int max_ctas = 0);
 int decode_cta_limit(const Shape &s);
 // Dense varlen plan (mstar.engine.resources.attn.dense, DensePlan): segment r's queries are
 // q[cu_q[r]..cu_q[r+1]), its keys rows cu_k[r]..cu_k[r+1] of contiguous K / V.

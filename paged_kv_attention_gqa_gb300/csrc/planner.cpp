@@ -214,7 +214,7 @@ static constexpr int kMinPagesPerCta = 2;
 
 void decode_split(const Shape &s, int rows, const int32_t *kvp, const int32_t *lpl, const int32_t *q_token,
                   const int32_t *out_token, int window_left, std::vector<DecodeTile> &tiles,
-                  std::vector<int32_t> &cta_ptr, std::vector<MergeRow> &merges, int &num_partials) {
+                  std::vector<int32_t> &cta_ptr, std::vector<MergeRow> &merges, int &num_partials, int max_ctas) {
     const int P = s.page_size;
     tiles.clear();
     cta_ptr.assign(1, 0);
@@ -233,7 +233,7 @@ void decode_split(const Shape &s, int rows, const int32_t *kvp, const int32_t *l
         W += vis[r];
     }
     if (W == 0) return;
-    long long cmax = decode_cta_limit(s);
+    long long cmax = max_ctas > 0 ? std::min(max_ctas, decode_cta_limit(s)) : decode_cta_limit(s);
     long long per = std::max<long long>((W + cmax - 1) / cmax, kMinPagesPerCta);
     int ctas = (int)((W + per - 1) / per);
     // Walk the rows' visible pages in order, cutting every `per` pages.
@@ -326,6 +326,28 @@ static void prefill_tiles(const Shape &s, const std::vector<int> &rows, const in
     for (int r : rows)
         prs.push_back(PrefillRow{qo[r + 1] - qo[r], row_len(kvp, lpl, r, s.page_size), q_begin_of_row[r], kvp[r]});
     prefill_tiles_rows(s, prs, causal, window_left, out);
+}
+
+// Time model of one GB300 used to share the SMs between the two passes of a mixed step:
+// streaming K/V at ~6.4 TB/s, prefill tiles at ~0.9 PFLOP/s (both measured on this
+// library's own kernels).
+constexpr double kDecodeBytesPerUs = 6.4e6;
+constexpr double kPrefillFlopsPerUs = 0.9e9;
+
+static int mixed_decode_ctas(const Shape &s, int rows, const int32_t *kvp, const int32_t *lpl, int window_left,
+                             const std::vector<PrefillTile> &ptiles) {
+    const int C = decode_cta_limit(s);
+    if (ptiles.empty()) return C;
+    double bytes = 0.0, flops = 0.0;
+    for (int r = 0; r < rows; ++r) {
+        const int L = row_len(kvp, lpl, r, s.page_size);
+        const int lo = window_left >= 0 ? std::max(0, L - 1 - window_left) : 0;
+        bytes += (double)(L - lo) * s.num_kv_heads * s.head_dim * 4.0;
+    }
+    for (const PrefillTile &t : ptiles) flops += 4.0 * kPrefillRowsPerTile * s.head_dim * (t.key_end - t.key_begin);
+    const double t_dec = bytes / kDecodeBytesPerUs, t_pf = flops / kPrefillFlopsPerUs;
+    const int pf_sms = (int)(C * t_pf / (t_dec + t_pf) + 0.5);
+    return std::max(C / 4, std::min(C, C - pf_sms));
 }
 
 static int prefill_tile_bound(const Shape &s, int rows, int tokens) {
@@ -495,12 +517,6 @@ int make_plan(const Shape &s, int mode, const int32_t *qo, const int32_t *kvp, c
             err = "sink_page outside the cache";
             return PKV_ERR_INVALID;
         }
-        // Decode pass over every row: a decode row attends its own pages, any other row
-        // one token of the sink page; the latter's result is dropped (out_token -1).
-        decode_split(s, batch, m.dec_kv_indptr.data(), m.dec_last_page_len.data(), m.dec_q_token.data(),
-                     m.dec_out_token.data(), window_left, dtiles, cta_ptr, merges, partials);
-        dec_pages = m.dec_kv_indices;
-        plan.dec_rows = batch;
         // Prefill pass over the prompt rows.  The permutation puts each prompt row's
         // tokens into one contiguous run of the permuted order; the run of prompt row k
         // starts at permuted index pf_qo_indptr[k], i.e. at original token
@@ -516,6 +532,16 @@ int make_plan(const Shape &s, int mode, const int32_t *qo, const int32_t *kvp, c
         }
         prefill_tiles(s, rows, qbeg.data(), qo, kvp, lpl, causal, window_left, ptiles);
         pf_pages.assign(kvi, kvi + kvp[batch]);
+        // Decode pass over every row: a decode row attends its own pages, any other row
+        // one token of the sink page; the latter's result is dropped (out_token -1).  The
+        // two passes run concurrently: the decode pass gets the SMs its bytes need, the
+        // prefill pass's CTAs fill the others.
+        decode_split(s, batch, m.dec_kv_indptr.data(), m.dec_last_page_len.data(), m.dec_q_token.data(),
+                     m.dec_out_token.data(), window_left, dtiles, cta_ptr, merges, partials,
+                     mixed_decode_ctas(s, batch, m.dec_kv_indptr.data(), m.dec_last_page_len.data(), window_left,
+                                       ptiles));
+        dec_pages = m.dec_kv_indices;
+        plan.dec_rows = batch;
     } else {
         err = "unknown plan mode";
         return PKV_ERR_INVALID;
