@@ -40,6 +40,7 @@ struct DecodeArgs {
     const int32_t *pages;
     float *part_o;
     float *part_lse;
+    MergeRow *merges;
     PlanHeader *hdr;  // per-plan values (error word, sm_scale) in the workspace
     int num_qo_heads;
     int num_kv_heads;
@@ -51,6 +52,45 @@ struct DecodeArgs {
 
 constexpr float kLn2 = 0.6931471805599453f;
 
+// Merge the split-KV partials of cut row `m` (at most kFusedMergeMaxPieces of them) for
+// the g heads of kv head `hk`, one warp: with w_j = exp(lse_j - max lse),
+// o = sum_j w_j o_j / sum_j w_j and lse = max + ln sum_j w_j.  Lane j holds piece j's lse.
+template <int D, int G>
+__device__ __forceinline__ void merge_row_heads(const struct DecodeArgs &a, int m, int hk, int lane) {
+    constexpr int C = D / 32;  // columns per lane
+    const MergeRow mr = a.merges[m];
+    const int Hq = a.num_qo_heads;
+    for (int gi = 0; gi < G; ++gi) {
+        const int h = hk * G + gi;
+        const float lj = lane < mr.count ? __ldcg(a.part_lse + (size_t)(mr.first + lane) * Hq + h) : -INFINITY;
+        float M = lj;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        const float wj = lane < mr.count ? __expf(lj - M) : 0.f;
+        float wsum = wj;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+        float acc[C];
+#pragma unroll
+        for (int c = 0; c < C; ++c) acc[c] = 0.f;
+#pragma unroll
+        for (int j = 0; j < kFusedMergeMaxPieces; ++j) {
+            const float w = __shfl_sync(0xffffffffu, wj, j);
+            if (j < mr.count) {
+                const float *src = a.part_o + ((size_t)(mr.first + j) * Hq + h) * D + lane * C;
+#pragma unroll
+                for (int c = 0; c < C; ++c) acc[c] += w * __ldcg(src + c);
+            }
+        }
+        if (mr.out_token < 0) continue;
+        const float inv = 1.f / wsum;
+        __nv_bfloat16 *dst = a.out + ((size_t)mr.out_token * Hq + h) * D + lane * C;
+#pragma unroll
+        for (int c = 0; c < C; c += 2) *reinterpret_cast<uint32_t *>(dst + c) = pack_bf16(acc[c] * inv, acc[c + 1] * inv);
+        if (a.lse && lane == 0) a.lse[(size_t)mr.out_token * Hq + h] = M + __logf(wsum);
+    }
+}
+
 template <int D, int G>
 __global__ void __launch_bounds__(9 * 32, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeArgs a) {
@@ -61,6 +101,7 @@ __global__ void __launch_bounds__(9 * 32, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)a.stages * a.stage_bytes);
     uint64_t *empty = full + a.stages;
+    volatile int *last_piece = reinterpret_cast<volatile int *>(empty + a.stages);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -71,6 +112,7 @@ __global__ void __launch_bounds__(9 * 32, 1)
     if (t_begin >= t_end) return;  // an idle CTA of a launch at the handle's maxima
     int *err = &a.hdr->err;
     const float scale_log2 = a.hdr->scale_log2;
+    const bool fused_merge = a.hdr->fused_merge != 0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < a.stages; ++s) {
@@ -130,6 +172,7 @@ __global__ void __launch_bounds__(9 * 32, 1)
     const int v_chk = lane >> 4;
 
     uint32_t it = 0;
+    bool ok = true;
     for (int ti = t_begin; ti < t_end; ++ti) {
         const DecodeTile t = a.tiles[ti];
         // Query fragments: rows = the g heads of this kv head (rows >= G are zero).
@@ -153,7 +196,9 @@ __global__ void __launch_bounds__(9 * 32, 1)
 
         for (int pi = t.page_begin; pi < t.page_begin + t.page_count; ++pi, ++it) {
             const int s = it % a.stages;
-            if (!mbar_wait(&full[s], (it / a.stages) & 1, err, kErrWaitFull)) return;
+            // a wait that gives up clears ok; the warp still walks its tiles so that the
+            // consumer warps keep meeting at their named barriers (no time limit there)
+            ok = ok && mbar_wait(&full[s], (it / a.stages) & 1, err, kErrWaitFull);
             uint8_t *st = smem + (size_t)s * a.stage_bytes;
             const uint32_t kbase = smem_u32(st);
             const uint32_t vbase = kbase + HALVES * a.box_bytes;
@@ -287,19 +332,36 @@ __global__ void __launch_bounds__(9 * 32, 1)
                 if (gid < G) a.part_lse[(size_t)t.partial * Hq + h0] = lse0;
                 if (gid + 8 < G) a.part_lse[(size_t)t.partial * Hq + h1] = lse1;
             }
+            // The CTA that finishes the last piece of a cut row merges its partials (a
+            // counter per row; fences order the partials before the count and the merge's
+            // reads after it) -- when the plan keeps merges in this kernel.
+            if (!fused_merge) continue;
+            __threadfence();
+            named_barrier_sync(1, Hkv * 32);
+            if (threadIdx.x == 0) {
+                MergeRow *mr = &a.merges[t.merge_row];
+                *last_piece = atomicAdd(&mr->arrived, 1) == mr->count - 1;
+            }
+            named_barrier_sync(1, Hkv * 32);
+            if (*last_piece) {
+                __threadfence();
+                merge_row_heads<D, G>(a, t.merge_row, hk, lane);
+                if (threadIdx.x == 0) a.merges[t.merge_row].arrived = 0;  // ready for the next run
+            }
         }
     }
 }
 
-// Merge the split-KV partials of each cut row: with w_j = exp(lse_j - max lse),
-// o = sum_j w_j o_j / sum_j w_j and lse = max lse + ln sum_j w_j.  Grid: (cut rows,
-// head groups); one thread per (head, 4 columns).
+// Merge the split-KV partials of each cut row when the plan does not fuse merges into the
+// decode kernel: with w_j = exp(lse_j - max lse), o = sum_j w_j o_j / sum_j w_j and
+// lse = max lse + ln sum_j w_j.  Grid: (cut rows, head groups); one thread per (head, 4
+// columns).
 constexpr int kMergeHeadsPerCta = 8;
 
 __global__ void __launch_bounds__(256) merge_kernel(const PlanHeader *hdr, const MergeRow *rows, const float *part_o,
                                                     const float *part_lse, __nv_bfloat16 *out, float *lse, int Hq,
                                                     int D) {
-    if ((int)blockIdx.x >= hdr->num_merge) return;
+    if (hdr->fused_merge || (int)blockIdx.x >= hdr->num_merge) return;
     const MergeRow mr = rows[blockIdx.x];
     if (mr.out_token < 0) return;
     const int per_head = D / 4;
@@ -325,22 +387,20 @@ __global__ void __launch_bounds__(256) merge_kernel(const PlanHeader *hdr, const
     if (lse && c == 0) lse[(size_t)mr.out_token * Hq + h] = M + __logf(wsum);
 }
 
-// Last-page append: one warp per new token copies its K and V rows (num_kv_heads x D
-// bf16 each) to slot rows[t] of the layer slice viewed as [pages * 2 * page_size] rows.
+
+// Last-page append: one thread per 16-byte chunk of a new token's K and V rows (num_kv_heads
+// x D bf16 each), all chunks in flight at once, written to slot rows[t] of the layer slice
+// viewed as [pages * 2 * page_size] rows (V rows page_size further).
 __global__ void __launch_bounds__(256) append_kernel(const PlanHeader *hdr, const uint4 *k, const uint4 *v, uint4 *cache,
                                                      const int32_t *rows, int vec_per_token, int page_size) {
-    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const int t = (int)(i / vec_per_token), c = (int)(i % vec_per_token);
     if (t >= hdr->num_append) return;
     const size_t row = (size_t)rows[t];
-    const int lane = threadIdx.x & 31;
-    const uint4 *ks = k + (size_t)t * vec_per_token;
-    const uint4 *vs = v + (size_t)t * vec_per_token;
-    uint4 *kd = cache + row * vec_per_token;
-    uint4 *vd = cache + (row + page_size) * vec_per_token;
-    for (int i = lane; i < vec_per_token; i += 32) {
-        kd[i] = ks[i];
-        vd[i] = vs[i];
-    }
+    const uint4 kk = k[(size_t)t * vec_per_token + c];
+    const uint4 vv = v[(size_t)t * vec_per_token + c];
+    cache[row * vec_per_token + c] = kk;
+    cache[(row + page_size) * vec_per_token + c] = vv;
 }
 
 // Gather of a frozen prefix (DenseAttentionManager): one warp per position t copies
@@ -388,7 +448,7 @@ int decode_stages(const Shape &s) {
 }
 
 size_t decode_smem_bytes(const Shape &s) {
-    return 1024 + (size_t)decode_stages(s) * decode_stage_bytes(s) + 2 * 8 * 8;
+    return 1024 + (size_t)decode_stages(s) * decode_stage_bytes(s) + 2 * 8 * 8 + 16;
 }
 
 // Raise a kernel's dynamic shared-memory limit; skipped while `st` is being captured
@@ -424,6 +484,7 @@ cudaError_t launch_decode(const Shape &s, const Plan &p, const CUtensorMap &tm, 
     a.pages = reinterpret_cast<const int32_t *>(w + p.lay.dec_pages);
     a.part_o = reinterpret_cast<float *>(w + p.lay.part_o);
     a.part_lse = reinterpret_cast<float *>(w + p.lay.part_lse);
+    a.merges = reinterpret_cast<MergeRow *>(w + p.lay.merge_rows);
     a.hdr = reinterpret_cast<PlanHeader *>(w + p.lay.err);
     a.num_qo_heads = s.num_qo_heads;
     a.num_kv_heads = s.num_kv_heads;
@@ -441,13 +502,14 @@ cudaError_t launch_decode(const Shape &s, const Plan &p, const CUtensorMap &tm, 
     PKV_DEC(128, 1) PKV_DEC(128, 2) PKV_DEC(128, 4) PKV_DEC(128, 8) PKV_DEC(128, 16)
 #undef PKV_DEC
     if (e != cudaSuccess) return e;
-    const int merges = s.graph_static ? sc.num_merge : p.num_merge;
+    // merges of rows cut into many pieces: a separate kernel (graph mode always launches it,
+    // and it returns at once when the plan merged inside the decode kernel)
+    const int merges = s.graph_static ? sc.num_merge : (p.fused_merge ? 0 : p.num_merge);
     if (merges) {
         const dim3 mgrid(merges, (s.num_qo_heads + dev::kMergeHeadsPerCta - 1) / dev::kMergeHeadsPerCta);
         dev::merge_kernel<<<mgrid, dev::kMergeHeadsPerCta * s.head_dim / 4, 0, st>>>(
-            a.hdr, reinterpret_cast<const MergeRow *>(w + p.lay.merge_rows),
-                                                        a.part_o, a.part_lse, a.out, lse, s.num_qo_heads,
-                                                        s.head_dim);
+            a.hdr, reinterpret_cast<const MergeRow *>(w + p.lay.merge_rows), a.part_o, a.part_lse, a.out, lse,
+            s.num_qo_heads, s.head_dim);
         e = cudaGetLastError();
     }
     return e;
@@ -459,9 +521,9 @@ cudaError_t launch_append(const Shape &s, const Plan &p, void *ws, const void *k
     if (tokens == 0) return cudaSuccess;
     uint8_t *w = static_cast<uint8_t *>(ws);
     const int vec = s.num_kv_heads * s.head_dim * 2 / 16;
-    const int warps_per_block = 8;
-    const int grid = (tokens + warps_per_block - 1) / warps_per_block;
-    dev::append_kernel<<<grid, warps_per_block * 32, 0, st>>>(
+    const long long chunks = (long long)tokens * vec;
+    const int grid = (int)((chunks + 255) / 256);
+    dev::append_kernel<<<grid, 256, 0, st>>>(
         reinterpret_cast<const PlanHeader *>(w + p.lay.err), static_cast<const uint4 *>(k),
         static_cast<const uint4 *>(v), static_cast<uint4 *>(kv_layer),
         reinterpret_cast<const int32_t *>(w + p.lay.append_rows), vec, s.page_size);

@@ -21,6 +21,10 @@ inline size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a
 constexpr int kPrefillRowsPerTile = 128;
 // Keys per prefill K/V stage (4 pages of 16).
 constexpr int kPrefillKeysPerStage = 64;
+// A cut decode row with at most this many pieces is merged inside the decode kernel by
+// the CTA that finishes its last piece; longer ones by the separate merge kernel, whose
+// CTAs spread one row's heads over many SMs.
+constexpr int kFusedMergeMaxPieces = 4;
 
 // First bytes of every plan in the workspace: the per-plan values the kernels read on
 // the device, so that launches captured into a CUDA graph stay valid for later plans
@@ -35,6 +39,7 @@ struct PlanHeader {
     int32_t window_left;
     float scale_log2;     // sm_scale * log2(e)
     int32_t dense;        // prefill tiles read contiguous K / V runs instead of pages
+    int32_t fused_merge;  // decode: the CTA finishing a cut row's last piece merges it
 };
 static_assert(sizeof(PlanHeader) <= kAlign, "the header fits its aligned slot");
 
@@ -48,16 +53,19 @@ struct DecodeTile {
     int32_t length;      // L of the row
     int32_t lo;          // first visible position
     int32_t partial;     // split-KV partial slot, -1 = this piece is the whole row
+    int32_t merge_row;   // the row's MergeRow when it is cut, else -1
+    int32_t pad[3];
 };
-static_assert(sizeof(DecodeTile) == 32, "DecodeTile is 8 ints");
+static_assert(sizeof(DecodeTile) == 48, "DecodeTile is 12 ints");
 
 // A row whose visible pages were split over several CTAs: its partials
-// [first, first + count) are merged into out_token.
+// [first, first + count) are merged into out_token by the CTA that finishes the last
+// piece (arrived counts finished pieces; the merging CTA sets it back to 0).
 struct MergeRow {
     int32_t out_token;
     int32_t first;
     int32_t count;
-    int32_t pad;
+    int32_t arrived;
 };
 
 // One prefill work tile: up to BQ consecutive new tokens of one row, all q heads of one
@@ -121,6 +129,7 @@ struct Plan {
     int dec_nnz = 0;
     int pf_nnz = 0;
     int dec_ctas = 0, dec_tiles = 0, num_partials = 0, num_merge = 0;
+    int fused_merge = 0;         // every cut row has few pieces: merged inside the decode kernel
     int pf_tiles = 0;
     PlanLayout lay;
     std::vector<uint8_t> image;

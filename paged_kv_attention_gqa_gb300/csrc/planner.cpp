@@ -22,6 +22,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstring>
+#include <map>
 
 #include "../../include/pkv.h"
 
@@ -253,6 +254,8 @@ void decode_split(const Shape &s, int rows, const int32_t *kvp, const int32_t *l
                 t.length = len[r];
                 t.lo = lo[r];
                 t.partial = -1;
+                t.merge_row = -1;
+                t.pad[0] = t.pad[1] = t.pad[2] = 0;
                 row_tiles[r].push_back((int)tiles.size());
                 tiles.push_back(t);
                 used += take;
@@ -271,8 +274,11 @@ void decode_split(const Shape &s, int rows, const int32_t *kvp, const int32_t *l
         m.out_token = out_token[rr];
         m.first = num_partials;
         m.count = (int)row_tiles[rr].size();
-        m.pad = rr;
-        for (int ti : row_tiles[rr]) tiles[ti].partial = num_partials++;
+        m.arrived = 0;
+        for (int ti : row_tiles[rr]) {
+            tiles[ti].partial = num_partials++;
+            tiles[ti].merge_row = (int)merges.size();
+        }
         merges.push_back(m);
     }
 }
@@ -313,8 +319,19 @@ static void prefill_tiles_rows(const Shape &s, const std::vector<PrefillRow> &ro
             }
         }
     }
-    // Longest first, so the hardware's in-order CTA dispatch approximates LPT.
-    std::stable_sort(out.begin(), out.end(), [](const PrefillTile &a, const PrefillTile &b) {
+    // Dispatch order: the q-tiles of one (row, kv head) next to each other, so the CTAs in
+    // flight together stream the same K/V pages and share them in L2; groups longest first
+    // (by their longest tile), and longest first inside a group, approximating LPT.
+    std::map<std::pair<int, int>, int> group_len;  // (kv_base, kv_head) -> longest key range
+    for (const PrefillTile &t : out) {
+        int &g = group_len[{t.kv_base, t.kv_head}];
+        g = std::max(g, t.key_end - t.key_begin);
+    }
+    std::stable_sort(out.begin(), out.end(), [&](const PrefillTile &a, const PrefillTile &b) {
+        const int ga = group_len[{a.kv_base, a.kv_head}], gb = group_len[{b.kv_base, b.kv_head}];
+        if (ga != gb) return ga > gb;
+        if (a.kv_base != b.kv_base) return a.kv_base < b.kv_base;
+        if (a.kv_head != b.kv_head) return a.kv_head < b.kv_head;
         return (a.key_end - a.key_begin) > (b.key_end - b.key_begin);
     });
 }
@@ -430,6 +447,9 @@ static void finish_plan(const Shape &s, Plan &plan, int T, int window_left, cons
     plan.dec_ctas = dtiles.empty() ? 0 : (int)cta_ptr.size() - 1;
     plan.num_merge = (int)merges.size();
     plan.num_partials = partials;
+    plan.fused_merge = 1;
+    for (const MergeRow &m : merges)
+        if (m.count > kFusedMergeMaxPieces) plan.fused_merge = 0;
     plan.pf_tiles = (int)ptiles.size();
     if (s.graph_static) {
         // fixed layout at the maxima: captured launches keep pointing at the right arrays;
@@ -456,6 +476,7 @@ static void finish_plan(const Shape &s, Plan &plan, int T, int window_left, cons
     hdr.window_left = window_left;
     hdr.scale_log2 = plan.sm_scale * 1.4426950408889634f;
     hdr.dense = mode == PKV_MODE_DENSE ? 1 : 0;
+    hdr.fused_merge = plan.fused_merge;
     put(plan.image, plan.lay.err, &hdr, 1);
     put(plan.image, plan.lay.append_rows, app.data(), app.size());
     put(plan.image, plan.lay.dec_pages, dec_pages.data(), dec_pages.size());
