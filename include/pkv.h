@@ -110,10 +110,11 @@ typedef struct {
 
 /*
  * Create a handle.  Host-only apart from the device query when sm_count == 0.
- * Returns PKV_ERR_UNSUPPORTED unless head_dim is 64 or 128, page_size is 16,
- * num_qo_heads is a multiple of num_kv_heads with a group of 1..16, and
- * num_kv_heads <= 16 (check_flashinfer_head_dim: the pages' kernels likewise reject
- * a head_dim they do not compute exactly).  PKV_ERR_INVALID on non-positive sizes.
+ * Returns PKV_ERR_UNSUPPORTED unless head_dim is 64, 128 or 256, page_size is a power
+ * of two from 1 to 1024, num_qo_heads is a multiple of num_kv_heads with a group size
+ * g of 1..8 or 16, and num_kv_heads <= 256 (check_flashinfer_head_dim: the pages'
+ * kernels likewise reject a head_dim they do not compute exactly).  PKV_ERR_INVALID on
+ * non-positive sizes.
  * *out is set only on PKV_OK.
  */
 pkv_status pkv_create(const pkv_config *cfg, pkv_handle_t *out);

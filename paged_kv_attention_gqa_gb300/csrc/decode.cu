@@ -6,18 +6,21 @@
 // lse = ln sum exp.
 //
 // Design for GB300:
-//  * A persistent grid of one CTA per SM.  The planner hands each CTA a contiguous run
-//    of the batch's visible pages (balanced to +-1 page); a row cut by a CTA boundary
-//    writes an fp32 partial (o normalised, lse) into the workspace, merged afterwards.
-//  * One page of ALL kv heads is contiguous in the cache (K: page_size x Hkv x D, then V),
-//    so a CTA streams whole pages: one producer thread issues 2 x D/64 TMA boxes per page
-//    (K and V, 64-column halves, 128-byte swizzle) into a ring of stages, completion on an
-//    mbarrier; consumers release a stage through a second mbarrier.
+//  * A persistent grid of one CTA per SM (x: runs of pages, y: groups of kv heads when a
+//    CTA cannot hold all of them).  The planner hands each CTA a contiguous run of the
+//    batch's visible pages (balanced to +-1 page); a row cut by a CTA boundary writes an
+//    fp32 partial (o normalised, lse) into the workspace, merged afterwards.
+//  * The slots of one page are contiguous for ALL kv heads (K: page_size x Hkv x D, then
+//    V), so a CTA streams 16-key chunks of its heads: one producer thread issues TMA
+//    boxes (64-column halves, 128-byte swizzle) into a ring of stages, completion on an
+//    mbarrier; consumers release a stage through a second mbarrier.  A chunk is one box
+//    of K and one of V (page size >= 16), two of each (8), or 16 / P boxes each holding
+//    a whole page's K and V rows (P < 8).
 //  * One consumer warp per kv head.  The g query heads of the group are the M dimension of
 //    a 16x8x16 bf16 tensor-core MMA (padded to 16 rows); keys are N for QK^T and K for PV.
 //    Online softmax in the exp2 domain with quad shuffles.
-//  * Slots past the row's end in its last page are zeroed in shared memory before PV
-//    (their scores are masked to -inf; zeroing V keeps 0 * NaN out of the MMA).
+//  * Slots of a chunk past the piece's end are zeroed in shared memory before PV (their
+//    scores are masked to -inf; zeroing V keeps 0 * NaN out of the MMA).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -44,13 +47,19 @@ struct DecodeArgs {
     PlanHeader *hdr;  // per-plan values (error word, sm_scale) in the workspace
     int num_qo_heads;
     int num_kv_heads;
+    int heads;         // kv heads per CTA; blockIdx.y selects the group
     int page_size;
+    int page_shift;    // log2 page_size
+    int box_rows;      // rows per head of one TMA box
+    int kpb_shift;     // log2 of the keys one box holds per head
+    int kv_in_box;     // 1: a box holds a page's K rows then its V rows
+    int box_stride;    // bytes between boxes in a stage
     int stages;
     uint32_t stage_bytes;
-    uint32_t box_bytes;
 };
 
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr int kDecodeMaxStages = 16;
 
 // Merge the split-KV partials of cut row `m` (at most kFusedMergeMaxPieces of them) for
 // the g heads of kv head `hk`, one warp: with w_j = exp(lse_j - max lse),
@@ -91,8 +100,35 @@ __device__ __forceinline__ void merge_row_heads(const struct DecodeArgs &a, int 
     }
 }
 
+// The 16-key chunks of a tile: keys [base + 16 k, base + 16 k + 16) for k in [k0, nk),
+// of which positions below `end` belong to the tile (its last page may be cut short by
+// the row's end).
+struct ChunkRange {
+    int base, end, k0, nk;
+};
+__device__ __forceinline__ ChunkRange chunk_range(const DecodeTile &t, int P) {
+    ChunkRange c;
+    c.base = t.page_begin * P;
+    c.end = min(t.length, (t.page_begin + t.page_count) * P);
+    c.k0 = (max(t.lo, c.base) - c.base) / kDecodeKeysPerStage;
+    c.nk = (c.end - c.base + kDecodeKeysPerStage - 1) / kDecodeKeysPerStage;
+    return c;
+}
+
+// Byte offset, inside one 64-column half of a stage, of key `tok` (0..15) of local head
+// `hk`, and its 128-byte swizzle phase.  `vrow` = P when V rows follow K rows in a box.
+struct RowAddr {
+    uint32_t off;
+    uint32_t phase;
+};
+__device__ __forceinline__ RowAddr key_row(const DecodeArgs &a, int hk, int tok, int vrow) {
+    const int b = tok >> a.kpb_shift;
+    const int row = hk * a.box_rows + vrow + (tok & ((1 << a.kpb_shift) - 1));
+    return RowAddr{(uint32_t)(b * a.box_stride + row * 128), (uint32_t)(row & 7)};
+}
+
 template <int D, int G>
-__global__ void __launch_bounds__(9 * 32, 1)
+__global__ void __launch_bounds__((D > 128 ? 4 : 8) * 32 + 32, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeArgs a) {
     constexpr int KS = D / 16;  // k-steps of QK^T
     constexpr int NT = D / 8;   // 8-wide output column tiles
@@ -105,7 +141,8 @@ __global__ void __launch_bounds__(9 * 32, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int Hkv = a.num_kv_heads;
+    const int Hc = a.heads;
+    const int hg = blockIdx.y;
     const int P = a.page_size;
     const int t_begin = a.cta_ptr[blockIdx.x];
     const int t_end = a.cta_ptr[blockIdx.x + 1];
@@ -113,40 +150,53 @@ __global__ void __launch_bounds__(9 * 32, 1)
     int *err = &a.hdr->err;
     const float scale_log2 = a.hdr->scale_log2;
     const bool fused_merge = a.hdr->fused_merge != 0;
+    // stage layout: [K or V][64-column half][box]; with K and V in one box: [half][box]
+    const int kpb = 1 << a.kpb_shift;
+    const int nb = kDecodeKeysPerStage / kpb;
+    const uint32_t half_stride = (uint32_t)nb * a.box_stride;
+    const uint32_t v_region = a.kv_in_box ? 0u : HALVES * half_stride;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < a.stages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], Hkv);
+            mbar_init(&empty[s], Hc);
         }
         fence_barrier_init();
     }
     __syncthreads();
 
-    if (warp == Hkv) {
+    if (warp == Hc) {
         // ---------------- producer ----------------
         if (lane == 0) {
             prefetch_tmap(&tmap);
+            const int nkv = a.kv_in_box ? 1 : 2;
+            const uint32_t box_bytes = (uint32_t)a.box_rows * Hc * 128;
             uint32_t it = 0;
             bool ok = true;
             for (int ti = t_begin; ti < t_end && ok; ++ti) {
                 const DecodeTile t = a.tiles[ti];
-                for (int pi = t.page_begin; pi < t.page_begin + t.page_count; ++pi, ++it) {
+                const ChunkRange cr = chunk_range(t, P);
+                for (int k = cr.k0; k < cr.nk; ++k, ++it) {
                     const int s = it % a.stages;
                     const uint32_t use = it / a.stages;
                     if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, err, kErrWaitEmpty)) {
                         ok = false;
                         break;
                     }
-                    const int page = a.pages[t.kv_base + pi];
+                    const int pos0 = cr.base + k * kDecodeKeysPerStage;
+                    const int nbox = min(nb, (cr.end - pos0 + kpb - 1) / kpb);
                     uint8_t *st = smem + (size_t)s * a.stage_bytes;
-                    mbar_arrive_expect_tx(&full[s], a.stage_bytes);
+                    mbar_arrive_expect_tx(&full[s], (uint32_t)(nbox * nkv * HALVES) * box_bytes);
+                    for (int b = 0; b < nbox; ++b) {
+                        const int pb = pos0 + b * kpb;
+                        const int page = a.pages[t.kv_base + (pb >> a.page_shift)];
+                        const int row = page * 2 * P + (pb & (P - 1));
+                        for (int kv = 0; kv < nkv; ++kv)
 #pragma unroll
-                    for (int kv = 0; kv < 2; ++kv)
-#pragma unroll
-                        for (int h = 0; h < HALVES; ++h)
-                            tma_load_3d(st + (kv * HALVES + h) * a.box_bytes, &tmap, &full[s], h * 64,
-                                        (page * 2 + kv) * P, 0);
+                            for (int h = 0; h < HALVES; ++h)
+                                tma_load_3d(st + (kv * HALVES + h) * half_stride + b * a.box_stride, &tmap, &full[s],
+                                            h * 64, row + kv * P, hg * Hc);
+                    }
                 }
             }
             // Drain: every stage issued must have been consumed before the CTA exits.
@@ -158,27 +208,33 @@ __global__ void __launch_bounds__(9 * 32, 1)
         }
         return;
     }
-    if (warp >= Hkv) return;
+    if (warp >= Hc) return;
 
-    // ---------------- consumers: warp = kv head ----------------
-    const int hk = warp;
+// ---------------- consumers: warp = kv head ----------------
+    const int hk = warp;               // kv head within the CTA's group (its row in a box)
+    const int hkg = hg * Hc + warp;    // kv head
     const int gid = lane >> 2;   // row of the MMA fragment (query head within the group)
     const int tid4 = lane & 3;
     const int Hq = a.num_qo_heads;
-    // ldmatrix lane roles
+    // ldmatrix lane roles: the key row each lane addresses and its 16-byte column chunk
     const int k_tok = (lane & 7) + ((lane >> 4) << 3);
     const int k_chk = (lane >> 3) & 1;
     const int v_tok = (lane & 7) + (((lane >> 3) & 1) << 3);
     const int v_chk = lane >> 4;
+    const int vrow = a.kv_in_box ? P : 0;
+    const RowAddr ka = key_row(a, hk, k_tok, 0);
+    RowAddr va = key_row(a, hk, v_tok, vrow);
+    va.off += v_region;
 
     uint32_t it = 0;
     bool ok = true;
     for (int ti = t_begin; ti < t_end; ++ti) {
         const DecodeTile t = a.tiles[ti];
+        const ChunkRange cr = chunk_range(t, P);
         // Query fragments: rows = the g heads of this kv head (rows >= G are zero).
         uint32_t qa[KS][4];
         {
-            const __nv_bfloat16 *qrow = a.q + ((size_t)t.q_token * Hq + (size_t)hk * G) * D;
+            const __nv_bfloat16 *qrow = a.q + ((size_t)t.q_token * Hq + (size_t)hkg * G) * D;
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
                 const int c0 = ks * 16 + tid4 * 2;
@@ -194,36 +250,34 @@ __global__ void __launch_bounds__(9 * 32, 1)
         for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
         float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
 
-        for (int pi = t.page_begin; pi < t.page_begin + t.page_count; ++pi, ++it) {
+        for (int k = cr.k0; k < cr.nk; ++k, ++it) {
             const int s = it % a.stages;
             // a wait that gives up clears ok; the warp still walks its tiles so that the
             // consumer warps keep meeting at their named barriers (no time limit there)
             ok = ok && mbar_wait(&full[s], (it / a.stages) & 1, err, kErrWaitFull);
             uint8_t *st = smem + (size_t)s * a.stage_bytes;
-            const uint32_t kbase = smem_u32(st);
-            const uint32_t vbase = kbase + HALVES * a.box_bytes;
-            const int pos0 = pi * P;
-            const int nvalid = t.length - pos0;  // slots holding tokens of this row
-            if (nvalid < P) {
-                // zero V rows past the row's end (stale or poisoned slots)
-                const int nz = (P - nvalid) * (D / 8);
+            const uint32_t sbase = smem_u32(st);
+            const int pos0 = cr.base + k * kDecodeKeysPerStage;
+            const int nvalid = cr.end - pos0;  // keys of this chunk inside the piece
+            if (nvalid < kDecodeKeysPerStage) {
+                // zero this head's V rows past the piece's end (stale, unloaded or poisoned)
+                const int nz = (kDecodeKeysPerStage - nvalid) * (D / 8);
                 for (int i = lane; i < nz; i += 32) {
-                    const int slot = nvalid + i / (D / 8);
+                    const RowAddr z = key_row(a, hk, nvalid + i / (D / 8), vrow);
                     const int chunk = i % (D / 8);
-                    const int row = hk * P + slot;
-                    *reinterpret_cast<uint4 *>(st + HALVES * a.box_bytes + (chunk >> 3) * a.box_bytes +
-                                               swz128(row, chunk & 7)) = make_uint4(0, 0, 0, 0);
+                    *reinterpret_cast<uint4 *>(st + v_region + (chunk >> 3) * half_stride + z.off +
+                                               (((chunk & 7) ^ z.phase) << 4)) = make_uint4(0, 0, 0, 0);
                 }
                 __syncwarp();
             }
-            // S = Q K^T over the page's 16 slots: two n-tiles of 8 keys.
+            // S = Q K^T over the chunk's 16 keys: two n-tiles of 8 keys.
             float sc[2][4];
 #pragma unroll
             for (int n = 0; n < 2; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
                 const int chunk = ks * 2 + k_chk;
-                const uint32_t addr = kbase + (chunk >> 3) * a.box_bytes + swz128(hk * P + k_tok, chunk & 7);
+                const uint32_t addr = sbase + (chunk >> 3) * half_stride + ka.off + (((chunk & 7) ^ ka.phase) << 4);
                 uint32_t b0, b1, b2, b3;
                 ldmatrix_x4(addr, b0, b1, b2, b3);
                 mma_bf16_16816(sc[0], qa[ks], b0, b1);
@@ -236,7 +290,7 @@ __global__ void __launch_bounds__(9 * 32, 1)
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int pos = pos0 + n * 8 + tid4 * 2 + e;
-                    const bool vis = pos >= t.lo && pos < t.length;
+                    const bool vis = pos >= t.lo && pos < cr.end;
                     sc[n][e] = vis ? sc[n][e] * scale_log2 : -INFINITY;
                     sc[n][e + 2] = vis ? sc[n][e + 2] * scale_log2 : -INFINITY;
                     mx0 = fmaxf(mx0, sc[n][e]);
@@ -280,13 +334,13 @@ __global__ void __launch_bounds__(9 * 32, 1)
 #pragma unroll
             for (int dj = 0; dj < D / 16; ++dj) {
                 const int chunk = dj * 2 + v_chk;
-                const uint32_t addr = vbase + (chunk >> 3) * a.box_bytes + swz128(hk * P + v_tok, chunk & 7);
+                const uint32_t addr = sbase + (chunk >> 3) * half_stride + va.off + (((chunk & 7) ^ va.phase) << 4);
                 uint32_t b0, b1, b2, b3;
                 ldmatrix_x4_trans(addr, b0, b1, b2, b3);
                 mma_bf16_16816(acc[2 * dj], pa, b0, b1);
                 mma_bf16_16816(acc[2 * dj + 1], pa, b2, b3);
             }
-            if (nvalid < P) fence_proxy_async_smem();
+            if (nvalid < kDecodeKeysPerStage) fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
         }
@@ -299,7 +353,7 @@ __global__ void __launch_bounds__(9 * 32, 1)
         const float inv0 = 1.f / l0, inv1 = 1.f / l1;
         const float lse0 = (m0 + __log2f(l0)) * kLn2;
         const float lse1 = (m1 + __log2f(l1)) * kLn2;
-        const int h0 = hk * G + gid, h1 = hk * G + gid + 8;
+        const int h0 = hkg * G + gid, h1 = hkg * G + gid + 8;
         if (t.partial < 0) {
             if (t.out_token >= 0) {
                 __nv_bfloat16 *o = a.out + (size_t)t.out_token * Hq * D;
@@ -335,17 +389,19 @@ __global__ void __launch_bounds__(9 * 32, 1)
             // The CTA that finishes the last piece of a cut row merges its partials (a
             // counter per row; fences order the partials before the count and the merge's
             // reads after it) -- when the plan keeps merges in this kernel.
+            // Every head group's CTA counts its piece; the last of all of them merges
+            // every kv head of the row.
             if (!fused_merge) continue;
             __threadfence();
-            named_barrier_sync(1, Hkv * 32);
+            named_barrier_sync(1, Hc * 32);
             if (threadIdx.x == 0) {
                 MergeRow *mr = &a.merges[t.merge_row];
-                *last_piece = atomicAdd(&mr->arrived, 1) == mr->count - 1;
+                *last_piece = atomicAdd(&mr->arrived, 1) == mr->count * (int)gridDim.y - 1;
             }
-            named_barrier_sync(1, Hkv * 32);
+            named_barrier_sync(1, Hc * 32);
             if (*last_piece) {
                 __threadfence();
-                merge_row_heads<D, G>(a, t.merge_row, hk, lane);
+                for (int h2 = hk; h2 < a.num_kv_heads; h2 += Hc) merge_row_heads<D, G>(a, t.merge_row, h2, lane);
                 if (threadIdx.x == 0) a.merges[t.merge_row].arrived = 0;  // ready for the next run
             }
         }
@@ -354,20 +410,20 @@ __global__ void __launch_bounds__(9 * 32, 1)
 
 // Merge the split-KV partials of each cut row when the plan does not fuse merges into the
 // decode kernel: with w_j = exp(lse_j - max lse), o = sum_j w_j o_j / sum_j w_j and
-// lse = max lse + ln sum_j w_j.  Grid: (cut rows, head groups); one thread per (head, 4
-// columns).
-constexpr int kMergeHeadsPerCta = 8;
+// lse = max lse + ln sum_j w_j.  Grid: (cut rows, head groups of 1024 / D heads); one
+// thread per (head, 4 columns), 256 threads.
+constexpr int kMergeThreads = 256;
 
-__global__ void __launch_bounds__(256) merge_kernel(const PlanHeader *hdr, const MergeRow *rows, const float *part_o,
-                                                    const float *part_lse, __nv_bfloat16 *out, float *lse, int Hq,
-                                                    int D) {
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const PlanHeader *hdr, const MergeRow *rows,
+                                                              const float *part_o, const float *part_lse,
+                                                              __nv_bfloat16 *out, float *lse, int Hq, int D) {
     if (hdr->fused_merge || (int)blockIdx.x >= hdr->num_merge) return;
     const MergeRow mr = rows[blockIdx.x];
     if (mr.out_token < 0) return;
     const int per_head = D / 4;
-    const int h = blockIdx.y * kMergeHeadsPerCta + threadIdx.x / per_head;
+    const int h = blockIdx.y * (kMergeThreads / per_head) + threadIdx.x / per_head;
     const int c = (threadIdx.x % per_head) * 4;
-    if (h >= Hq || threadIdx.x >= kMergeHeadsPerCta * per_head) return;
+    if (h >= Hq) return;
     float M = -INFINITY;
     for (int j = 0; j < mr.count; ++j) M = fmaxf(M, part_lse[(size_t)(mr.first + j) * Hq + h]);
     float wsum = 0.f;
@@ -438,17 +494,19 @@ cudaError_t launch_gather(const Shape &s, const void *kv_layer, const int32_t *p
 }
 
 static uint32_t decode_stage_bytes(const Shape &s) {
-    return 2u * (uint32_t)s.page_size * s.num_kv_heads * s.head_dim * 2u;
+    const uint32_t boxes = kDecodeKeysPerStage / s.dec_keys_per_box();
+    const uint32_t kv = s.dec_kv_in_box() ? 1u : 2u;
+    return kv * (uint32_t)(s.head_dim / 64) * boxes * (uint32_t)s.dec_box_stride();
 }
 
 int decode_stages(const Shape &s) {
     const uint32_t sb = decode_stage_bytes(s);
     int st = (int)((200u * 1024u) / sb);
-    return st < 2 ? 0 : (st > 8 ? 8 : st);
+    return st < 2 ? 0 : (st > dev::kDecodeMaxStages ? dev::kDecodeMaxStages : st);
 }
 
 size_t decode_smem_bytes(const Shape &s) {
-    return 1024 + (size_t)decode_stages(s) * decode_stage_bytes(s) + 2 * 8 * 8 + 16;
+    return 1024 + (size_t)decode_stages(s) * decode_stage_bytes(s) + 2 * 8 * dev::kDecodeMaxStages + 16;
 }
 
 // Raise a kernel's dynamic shared-memory limit; skipped while `st` is being captured
@@ -460,7 +518,7 @@ cudaError_t set_smem_limit(const void *fn, size_t smem, cudaStream_t st) {
 }
 
 template <int D, int G>
-static cudaError_t launch_decode_t(const CUtensorMap &tm, const dev::DecodeArgs &a, int grid, int warps, size_t smem,
+static cudaError_t launch_decode_t(const CUtensorMap &tm, const dev::DecodeArgs &a, dim3 grid, int warps, size_t smem,
                                    cudaStream_t st) {
     auto fn = dev::decode_kernel<D, G>;
     cudaError_t e = set_smem_limit((const void *)fn, smem, st);
@@ -488,26 +546,32 @@ cudaError_t launch_decode(const Shape &s, const Plan &p, const CUtensorMap &tm, 
     a.hdr = reinterpret_cast<PlanHeader *>(w + p.lay.err);
     a.num_qo_heads = s.num_qo_heads;
     a.num_kv_heads = s.num_kv_heads;
+    a.heads = s.dec_heads();
     a.page_size = s.page_size;
+    a.page_shift = s.page_shift();
+    a.box_rows = s.dec_box_rows();
+    a.kpb_shift = __builtin_ctz((unsigned)s.dec_keys_per_box());
+    a.kv_in_box = s.dec_kv_in_box() ? 1 : 0;
+    a.box_stride = s.dec_box_stride();
     a.stages = decode_stages(s);
     a.stage_bytes = decode_stage_bytes(s);
-    a.box_bytes = (uint32_t)s.page_size * s.num_kv_heads * 128u;
-    const int warps = s.num_kv_heads + 1;
+    if (a.stages == 0) return cudaErrorInvalidValue;
+    const int warps = a.heads + 1;
     const size_t smem = decode_smem_bytes(s);
     cudaError_t e = cudaErrorInvalidValue;
     const int g = s.group();
 #define PKV_DEC(DD, GG) \
-    if (s.head_dim == DD && g == GG) e = launch_decode_t<DD, GG>(tm, a, grid, warps, smem, st);
-    PKV_DEC(64, 1) PKV_DEC(64, 2) PKV_DEC(64, 4) PKV_DEC(64, 8) PKV_DEC(64, 16)
-    PKV_DEC(128, 1) PKV_DEC(128, 2) PKV_DEC(128, 4) PKV_DEC(128, 8) PKV_DEC(128, 16)
+    if (s.head_dim == DD && g == GG) e = launch_decode_t<DD, GG>(tm, a, dim3(grid, s.dec_head_groups()), warps, smem, st);
+    PKV_FOR_EACH_HEAD_DIM_AND_GROUP(PKV_DEC)
 #undef PKV_DEC
     if (e != cudaSuccess) return e;
     // merges of rows cut into many pieces: a separate kernel (graph mode always launches it,
     // and it returns at once when the plan merged inside the decode kernel)
     const int merges = s.graph_static ? sc.num_merge : (p.fused_merge ? 0 : p.num_merge);
     if (merges) {
-        const dim3 mgrid(merges, (s.num_qo_heads + dev::kMergeHeadsPerCta - 1) / dev::kMergeHeadsPerCta);
-        dev::merge_kernel<<<mgrid, dev::kMergeHeadsPerCta * s.head_dim / 4, 0, st>>>(
+        const int heads_per_cta = dev::kMergeThreads / (s.head_dim / 4);
+        const dim3 mgrid(merges, (s.num_qo_heads + heads_per_cta - 1) / heads_per_cta);
+        dev::merge_kernel<<<mgrid, dev::kMergeThreads, 0, st>>>(
             a.hdr, reinterpret_cast<const MergeRow *>(w + p.lay.merge_rows), a.part_o, a.part_lse, a.out, lse,
             s.num_qo_heads, s.head_dim);
         e = cudaGetLastError();

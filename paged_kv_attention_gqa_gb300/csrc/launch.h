@@ -5,6 +5,10 @@
 
 #include "plan.h"
 
+// Every (head_dim, group size) the kernels are compiled for.
+#define PKV_FOR_EACH_GROUP(X, DD) X(DD, 1) X(DD, 2) X(DD, 3) X(DD, 4) X(DD, 5) X(DD, 6) X(DD, 7) X(DD, 8) X(DD, 16)
+#define PKV_FOR_EACH_HEAD_DIM_AND_GROUP(X) PKV_FOR_EACH_GROUP(X, 64) PKV_FOR_EACH_GROUP(X, 128) PKV_FOR_EACH_GROUP(X, 256)
+
 namespace pkv {
 
 int decode_stages(const Shape &s);
@@ -14,16 +18,18 @@ size_t prefill_smem_bytes(const Shape &s);
 
 cudaError_t launch_append(const Shape &s, const Plan &p, void *ws, const void *k, const void *v, void *kv_layer,
                           cudaStream_t st);
-// Decode pass (and the split-KV merge) of a DECODE or MIXED plan; `tm` boxes a whole
-// page of all kv heads.
+// Decode pass (and the split-KV merge) of a DECODE or MIXED plan; `tm` boxes
+// (64 columns, Shape::dec_box_rows() rows, Shape::dec_heads() heads) of the layer slice.
 cudaError_t launch_decode(const Shape &s, const Plan &p, const CUtensorMap &tm, void *ws, const void *q, void *out,
                           float *lse, cudaStream_t st);
-// Prefill pass of a PREFILL, MIXED or DENSE plan; `tm_kv` boxes 16 rows of one kv head of
-// the layer slice (paged; V rows follow K rows by page_size) or of contiguous K (dense,
-// with `tm_v` over contiguous V); `tm_q` boxes (64 columns, g heads, 128/g tokens) of q
-// viewed as [tokens][Hq][D].
+// Prefill pass of a PREFILL, MIXED or DENSE plan; `tm_kv` boxes Shape::pf_box_rows() rows
+// of one kv head of the layer slice (paged; V rows follow K rows by page_size) or 16 rows
+// of contiguous K (dense, with `tm_v` over contiguous V); `tm_q` boxes (64 columns, g
+// heads, 128/g tokens) of q viewed as [tokens][Hq][D].  Paged plans with pages smaller than
+// 8 slots read `kv_layer` directly (16-byte copies) instead of `tm_kv`.
 cudaError_t launch_prefill(const Shape &s, const Plan &p, const CUtensorMap &tm_kv, const CUtensorMap &tm_v,
-                           const CUtensorMap &tm_q, void *ws, void *out, float *lse, cudaStream_t st);
+                           const CUtensorMap &tm_q, const void *kv_layer, void *ws, void *out, float *lse,
+                           cudaStream_t st);
 // Copy the first `num_tokens` positions of a page list into contiguous K and V
 // ([num_tokens, Hkv, D] each).
 cudaError_t launch_gather(const Shape &s, const void *kv_layer, const int32_t *pages, int num_tokens, void *k_out,

@@ -58,17 +58,18 @@ extern "C" pkv_status pkv_create(const pkv_config *cfg, pkv_handle_t *out) {
         c.max_total_tokens < 0 || c.max_num_pages <= 0 || c.num_cache_pages <= 0 || c.max_prefill_rows < 0 ||
         c.sm_count < 0)
         return fail(nullptr, PKV_ERR_INVALID, "configuration sizes must be positive");
-    if (c.head_dim != 64 && c.head_dim != 128)
-        return fail(nullptr, PKV_ERR_UNSUPPORTED, "head_dim " + std::to_string(c.head_dim) + " is not computed (64, 128)");
-    if (c.page_size != 16)
-        return fail(nullptr, PKV_ERR_UNSUPPORTED, "page_size " + std::to_string(c.page_size) + " is not computed (16)");
+    if (c.head_dim != 64 && c.head_dim != 128 && c.head_dim != 256)
+        return fail(nullptr, PKV_ERR_UNSUPPORTED,
+                    "head_dim " + std::to_string(c.head_dim) + " is not computed (64, 128, 256)");
+    if ((c.page_size & (c.page_size - 1)) != 0 || c.page_size > 1024)
+        return fail(nullptr, PKV_ERR_UNSUPPORTED,
+                    "page_size " + std::to_string(c.page_size) + " is not computed (a power of two up to 1024)");
     if (c.num_qo_heads % c.num_kv_heads != 0)
         return fail(nullptr, PKV_ERR_UNSUPPORTED, "num_qo_heads must be a multiple of num_kv_heads");
     const int g = c.num_qo_heads / c.num_kv_heads;
-    if (g != 1 && g != 2 && g != 4 && g != 8 && g != 16)
-        return fail(nullptr, PKV_ERR_UNSUPPORTED, "group size " + std::to_string(g) + " is not computed (1,2,4,8,16)");
-    if (c.num_kv_heads > 8)
-        return fail(nullptr, PKV_ERR_UNSUPPORTED, "num_kv_heads above 8 is not computed");
+    if (!((g >= 1 && g <= 8) || g == 16))
+        return fail(nullptr, PKV_ERR_UNSUPPORTED, "group size " + std::to_string(g) + " is not computed (1..8, 16)");
+    if (c.num_kv_heads > 256) return fail(nullptr, PKV_ERR_UNSUPPORTED, "num_kv_heads above 256 is not computed");
     if (c.sink_page >= c.num_cache_pages)
         return fail(nullptr, PKV_ERR_INVALID, "sink_page outside the cache");
     if (c.graph_static != 0 && c.graph_static != 1) return fail(nullptr, PKV_ERR_INVALID, "graph_static is 0 or 1");
@@ -194,25 +195,28 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // Tensor map over one layer slice viewed as [Hkv][pages * 2 * page_size rows][D] with the
-// head dimension OUTERMOST, so that a box of (64 columns, page_size slots, heads) lands
+// head dimension OUTERMOST, so that a box of (64 columns, box_rows slots, heads) lands
 // in shared memory head-major: each head's slots are consecutive 128-byte rows.
-static pkv_status encode_rows(pkv_handle_t h, const void *base, long long rows, int box_heads, CUtensorMap *tm);
+static pkv_status encode_rows(pkv_handle_t h, const void *base, long long rows, int box_rows, int box_heads,
+                              CUtensorMap *tm);
 
-static pkv_status encode_kv(pkv_handle_t h, const void *kv_layer, int box_heads, CUtensorMap *tm) {
-    return encode_rows(h, kv_layer, (long long)h->shape.num_cache_pages * 2 * h->shape.page_size, box_heads, tm);
+static pkv_status encode_kv(pkv_handle_t h, const void *kv_layer, int box_rows, int box_heads, CUtensorMap *tm) {
+    return encode_rows(h, kv_layer, (long long)h->shape.num_cache_pages * 2 * h->shape.page_size, box_rows, box_heads,
+                       tm);
 }
 
 // Tensor map over [rows][Hkv][D] bf16 rows of Hkv*D elements (a layer slice viewed as
-// pages*2*page_size rows, or a contiguous K or V tensor), boxes of (64 columns, 16 rows,
-// box_heads heads), heads outermost so that one head's rows land contiguously.
-static pkv_status encode_rows(pkv_handle_t h, const void *kv_layer, long long rows, int box_heads, CUtensorMap *tm) {
+// pages*2*page_size rows, or a contiguous K or V tensor), boxes of (64 columns, box_rows
+// rows, box_heads heads), heads outermost so that one head's rows land contiguously.
+static pkv_status encode_rows(pkv_handle_t h, const void *kv_layer, long long rows, int box_rows, int box_heads,
+                              CUtensorMap *tm) {
     auto fn = encode_fn();
     if (!fn) return fail(h, PKV_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
     const Shape &s = h->shape;
     if (reinterpret_cast<uintptr_t>(kv_layer) % 16) return fail(h, PKV_ERR_INVALID, "kv_layer must be 16-byte aligned");
     cuuint64_t dims[3] = {(cuuint64_t)s.head_dim, (cuuint64_t)rows, (cuuint64_t)s.num_kv_heads};
     cuuint64_t strides[2] = {(cuuint64_t)s.num_kv_heads * s.head_dim * 2, (cuuint64_t)s.head_dim * 2};
-    cuuint32_t box[3] = {64, (cuuint32_t)s.page_size, (cuuint32_t)box_heads};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, (cuuint32_t)box_heads};
     if (rows < 1) return fail(h, PKV_ERR_INVALID, "a K / V tensor needs at least one row");
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(kv_layer), dims, strides, box, estr,
@@ -260,14 +264,15 @@ static pkv_status check_planned(pkv_handle_t h, void *ws, int mode_a, int mode_b
 
 static pkv_status dec_map(pkv_handle_t h, const void *kv) {
     if (h->tm_dec_ptr == kv) return PKV_OK;
-    pkv_status st = encode_kv(h, kv, h->shape.num_kv_heads, &h->tm_dec);
+    pkv_status st = encode_kv(h, kv, h->shape.dec_box_rows(), h->shape.dec_heads(), &h->tm_dec);
     if (st == PKV_OK) h->tm_dec_ptr = kv;
     return st;
 }
 
 static pkv_status pf_map(pkv_handle_t h, const void *kv) {
     if (h->tm_pf_ptr == kv) return PKV_OK;
-    pkv_status st = encode_kv(h, kv, 1, &h->tm_pf);
+    // pages below 8 slots are gathered by the kernel; the map is then unused
+    pkv_status st = encode_kv(h, kv, h->shape.pf_box_rows(), 1, &h->tm_pf);
     if (st == PKV_OK) h->tm_pf_ptr = kv;
     return st;
 }
@@ -311,7 +316,7 @@ extern "C" pkv_status pkv_run_prefill(pkv_handle_t h, const void *q, const void 
     if ((st = check_io(h, q, kv_layer, out)) != PKV_OK) return st;
     if ((st = pf_map(h, kv_layer)) != PKV_OK) return st;
     if ((st = q_map(h, q, q_rows(h))) != PKV_OK) return st;
-    cudaError_t e = pkv::launch_prefill(h->shape, h->plan, h->tm_pf, h->tm_pf, h->tm_q, workspace, out, lse,
+    cudaError_t e = pkv::launch_prefill(h->shape, h->plan, h->tm_pf, h->tm_pf, h->tm_q, kv_layer, workspace, out, lse,
                                         static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PKV_OK : cuda_fail(h, e, "prefill launch");
 }
@@ -341,7 +346,7 @@ extern "C" pkv_status pkv_run_mixed(pkv_handle_t h, const void *q, const void *k
     if (e != cudaSuccess) return cuda_fail(h, e, "mixed fork");
     e = pkv::launch_decode(h->shape, h->plan, h->tm_dec, workspace, q, out, lse, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "mixed decode-pass launch");
-    e = pkv::launch_prefill(h->shape, h->plan, h->tm_pf, h->tm_pf, h->tm_q, workspace, out, lse, h->side);
+    e = pkv::launch_prefill(h->shape, h->plan, h->tm_pf, h->tm_pf, h->tm_q, kv_layer, workspace, out, lse, h->side);
     if (e != cudaSuccess) return cuda_fail(h, e, "mixed prefill-pass launch");
     e = cudaEventRecord(h->ev_join, h->side);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(s, h->ev_join, 0);
@@ -499,10 +504,10 @@ extern "C" pkv_status pkv_run_dense(pkv_handle_t h, const void *q, const void *k
     if (!v || (reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) % 16)
         return fail(h, PKV_ERR_INVALID, "k and v must be non-null and 16-byte aligned");
     CUtensorMap tk, tv;
-    if ((st = encode_rows(h, k, h->plan.num_keys, 1, &tk)) != PKV_OK) return st;
-    if ((st = encode_rows(h, v, h->plan.num_keys, 1, &tv)) != PKV_OK) return st;
+    if ((st = encode_rows(h, k, h->plan.num_keys, 16, 1, &tk)) != PKV_OK) return st;
+    if ((st = encode_rows(h, v, h->plan.num_keys, 16, 1, &tv)) != PKV_OK) return st;
     if ((st = q_map(h, q, h->plan.num_tokens)) != PKV_OK) return st;
-    cudaError_t e = pkv::launch_prefill(h->shape, h->plan, tk, tv, h->tm_q, workspace, out, lse,
+    cudaError_t e = pkv::launch_prefill(h->shape, h->plan, tk, tv, h->tm_q, nullptr, workspace, out, lse,
                                         static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PKV_OK : cuda_fail(h, e, "dense launch");
 }

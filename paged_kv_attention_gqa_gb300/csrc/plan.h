@@ -19,8 +19,10 @@ inline size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a
 
 // Query rows of one prefill tile: BQ tokens x all g q-heads of one kv head.
 constexpr int kPrefillRowsPerTile = 128;
-// Keys per prefill K/V stage (4 pages of 16).
+// Keys per prefill K/V stage.
 constexpr int kPrefillKeysPerStage = 64;
+// Keys per decode stage (one ring slot): two 8-key n-tiles of the QK^T MMA.
+constexpr int kDecodeKeysPerStage = 16;
 // A cut decode row with at most this many pieces is merged inside the decode kernel by
 // the CTA that finishes its last piece; longer ones by the separate merge kernel, whose
 // CTAs spread one row's heads over many SMs.
@@ -105,6 +107,32 @@ struct Shape {
     int sm_count, sink_page;
     int graph_static;  // launch at the maxima with a fixed workspace layout (CUDA-graph mode)
     int group() const { return num_qo_heads / num_kv_heads; }
+    // page_size is a power of two: slot = position & (P - 1), page = position >> shift
+    int page_shift() const { return __builtin_ctz((unsigned)page_size); }
+
+    // Decode: kv heads one CTA streams (one consumer warp each): the largest divisor of
+    // num_kv_heads up to 8 (4 at head_dim 256, whose accumulators take twice the
+    // registers); the kv heads are split into dec_head_groups() groups over the grid's y.
+    int dec_heads() const {
+        const int cap = head_dim > 128 ? 4 : 8;
+        for (int d = cap < num_kv_heads ? cap : num_kv_heads; d > 1; --d)
+            if (num_kv_heads % d == 0) return d;
+        return 1;
+    }
+    int dec_head_groups() const { return num_kv_heads / dec_heads(); }
+    // Decode TMA boxes (64 columns x rows x dec_heads() heads, heads outermost).  From page
+    // size 8 up a box holds min(P, 16) slots of K, and another the same slots of V; below
+    // 8 one box holds a whole page, its P K rows followed by its P V rows (adjacent in the
+    // cache), so that a box is never smaller than 8 rows for 8 heads.
+    bool dec_kv_in_box() const { return page_size < 8; }
+    int dec_keys_per_box() const { return page_size < 16 ? page_size : 16; }
+    int dec_box_rows() const { return dec_kv_in_box() ? 2 * page_size : dec_keys_per_box(); }
+    // Bytes between boxes in shared memory: each box starts on a 1024-byte swizzle atom.
+    int dec_box_stride() const { return (dec_box_rows() * dec_heads() * 128 + 1023) / 1024 * 1024; }
+    // Prefill: rows of one paged TMA box (one head); pages smaller than 8 slots are
+    // gathered with 16-byte cp.async copies instead (a box would not fill a swizzle atom).
+    bool pf_gather() const { return page_size < 8; }
+    int pf_box_rows() const { return page_size < 16 ? page_size : 16; }
 };
 
 // Worst-case counts at a handle's maxima for one plan mode: the launch grids and the

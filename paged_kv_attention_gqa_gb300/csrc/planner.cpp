@@ -205,13 +205,14 @@ int mixed_layout(const int32_t *qo, const int32_t *kvp, const int32_t *kvi, cons
 }
 
 int decode_cta_limit(const Shape &s) {
-    // One persistent decode CTA per SM: each holds a multi-page ring of whole pages.
-    return std::max(1, s.sm_count);
+    // One persistent decode CTA per SM: each holds a multi-stage ring of 16-key chunks of
+    // its kv heads; with several head groups the SMs are shared among them.
+    return std::max(1, s.sm_count / s.dec_head_groups());
 }
 
-// Pages each decode CTA is given at least (fewer pages per CTA would only multiply
-// partials without shortening the critical path).
-static constexpr int kMinPagesPerCta = 2;
+// Keys each decode CTA is given at least (fewer per CTA would only multiply partials
+// without shortening the critical path), rounded up to whole pages.
+static constexpr int kMinKeysPerCta = 32;
 
 void decode_split(const Shape &s, int rows, const int32_t *kvp, const int32_t *lpl, const int32_t *q_token,
                   const int32_t *out_token, int window_left, std::vector<DecodeTile> &tiles,
@@ -235,7 +236,8 @@ void decode_split(const Shape &s, int rows, const int32_t *kvp, const int32_t *l
     }
     if (W == 0) return;
     long long cmax = max_ctas > 0 ? std::min(max_ctas, decode_cta_limit(s)) : decode_cta_limit(s);
-    long long per = std::max<long long>((W + cmax - 1) / cmax, kMinPagesPerCta);
+    const long long min_pages = (kMinKeysPerCta + P - 1) / P;
+    long long per = std::max<long long>((W + cmax - 1) / cmax, min_pages);
     int ctas = (int)((W + per - 1) / per);
     // Walk the rows' visible pages in order, cutting every `per` pages.
     std::vector<std::vector<int>> row_tiles(rows);

@@ -8,12 +8,15 @@
 // A CTA computes one tile: up to BQ = 128 / g consecutive new tokens of one row times
 // the g query heads of one kv head = 128 query rows (row m = token * g + head), which
 // share every K/V tile.  Blackwell design, two CTAs per SM:
-//  * warp 4 (one thread) loads Q once and streams 64-key K and V tiles (four 16-slot
-//    pages of the kv head, 64-column halves, 128-byte swizzle) by TMA into a two-stage
+//  * warp 4 (one thread) loads Q once and streams 64-key K and V tiles (boxes of 16 or 8
+//    slots of the kv head, 64-column halves, 128-byte swizzle) by TMA into a two-stage
 //    ring; a page past the row's end is fetched at an out-of-range coordinate, which TMA
-//    fills with zeros;
-//  * warp 5 owns 256 tensor-memory columns: S double-buffered (2 x 64 fp32 columns) and
-//    O (D fp32 columns); one thread issues S_j = Q K_j^T (tcgen05.mma, both operands in
+//    fills with zeros.  Pages of 1, 2 or 4 slots are gathered instead by the whole warp
+//    with 16-byte cp.async copies into the same swizzled layout (keys past the row's end
+//    zero-filled);
+//  * warp 5 owns 256 tensor-memory columns (512 at head_dim 256): S double-buffered
+//    (2 x 64 fp32 columns) and O (D fp32 columns); one thread issues S_j = Q K_j^T
+//    (tcgen05.mma, both operands in
 //    shared memory, K-major) and then O += P_{j-1} V_{j-1} (P read from tensor memory,
 //    V from shared memory MN-major), committing each group to mbarriers;
 //  * warps 0-3 (thread = query row = TMEM lane) read S, mask, run the online softmax in
@@ -25,6 +28,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "../../include/pkv.h"
 #include "launch.h"
 #include "plan.h"
 #include "ptx.cuh"
@@ -39,15 +43,29 @@ struct PrefillArgs {
     const PrefillTile *tiles;
     const int32_t *pages;
     PlanHeader *hdr;  // per-plan values (tile count, causal, window, sm_scale) in the workspace
+    const uint8_t *kv_layer;  // the layer slice, for the cp.async gather of small pages
     int num_qo_heads;
+    int num_kv_heads;
     int page_size;
-    int oob_row;  // a row coordinate past the cache: TMA fills it with zeros
+    int page_shift;  // log2 page_size
+    int box_rows;  // rows of one paged TMA box (16, or 8 for 8-slot pages)
+    int gather;    // pages below 8 slots: cp.async gather instead of TMA
+    int oob_row;   // a row coordinate past the cache: TMA fills it with zeros
+};
+
+template <int N>
+struct IntConst {
+    static constexpr int value = N;
 };
 
 constexpr int kPfThreads = 192;  // warps 0-3 softmax, 4 producer, 5 MMA
 constexpr int kPfKeys = kPrefillKeysPerStage;  // 64 keys per K/V tile
 constexpr int kPfStages = 2;
-constexpr uint32_t kPfTmemCols = 256;
+// tensor-memory columns a CTA allocates: S (2 x 64) + O (D), rounded up to a power of two
+template <int D>
+struct PfTmem {
+    static constexpr uint32_t COLS = D > 128 ? 512u : 256u;
+};
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kLn2f = 0.6931471805599453f;
 
@@ -64,13 +82,15 @@ struct PfSmem {
 };
 
 template <int D, int G>
-__global__ void __launch_bounds__(kPfThreads, 2)
+__global__ void __launch_bounds__(kPfThreads, D > 128 ? 1 : 2)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ CUtensorMap tm_q, const PrefillArgs a) {
     using L = PfSmem<D>;
     constexpr int HALVES = L::HALVES;
     constexpr int BQ = kPrefillRowsPerTile / G;
+    constexpr uint32_t Q_TX = (uint32_t)BQ * G * D * 2;  // rows BQ*G..127 stay unused
     constexpr int KSTEPS = D / 16;
+    constexpr uint32_t kTmemCols = PfTmem<D>::COLS;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::BAR_OFF);
@@ -119,7 +139,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
         fence_barrier_init();
     }
     if (warp == 5) {
-        tmem_alloc(tmem_holder, kPfTmemCols);
+        tmem_alloc(tmem_holder, kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -131,46 +151,126 @@ __global__ void __launch_bounds__(kPfThreads, 2)
 
     if (warp == 4) {
         // ------------------------------------------------ producer
+        if constexpr (BQ * G < kPrefillRowsPerTile) {
+            // a group size that does not divide 128 leaves Q rows BQ*G..127 unloaded: zero
+            // them (their S rows are never stored, but must not hold Inf or NaN)
+            constexpr int ZROWS = kPrefillRowsPerTile - BQ * G;
+            for (int i = lane; i < HALVES * ZROWS * 8; i += 32) {
+                const int h = i / (ZROWS * 8), r = BQ * G + (i / 8) % ZROWS, c = i % 8;
+                *reinterpret_cast<uint4 *>(sm + L::Q_OFF + h * (L::Q_BYTES / HALVES) + r * 128 + c * 16) =
+                    make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+        }
         if (lane == 0) {
             prefetch_tmap(&tm_kv);
             prefetch_tmap(&tm_v);
             prefetch_tmap(&tm_q);
-            mbar_arrive_expect_tx(q_full, L::Q_BYTES);
+            mbar_arrive_expect_tx(q_full, Q_TX);
 #pragma unroll
             for (int h = 0; h < HALVES; ++h)
                 tma_load_3d(sm + L::Q_OFF + h * (L::Q_BYTES / HALVES), &tm_q, q_full, h * 64, t.kv_head * G,
                             t.q_begin);
-            const int npages = (t.length + P - 1) / P;
+        }
+        const int npages = (t.length + P - 1) >> a.page_shift;
+        if (!a.gather || dense) {
+            // TMA: a 64-key tile is NB boxes of 64 / NB rows (16, or 8 for 8-slot pages)
+            auto stream_tiles = [&](auto nb) {
+                constexpr int NB = decltype(nb)::value;
+                constexpr int R = kPfKeys / NB;
+                // cache rows of tile j's boxes (-1: past the row's pages)
+                auto tile_rows = [&](int j, int (&rows)[NB]) {
+                    const int key0 = (kt0 + j) * kPfKeys;
+#pragma unroll
+                    for (int b = 0; b < NB; ++b) {
+                        const int kb = key0 + b * R;
+                        if (dense)
+                            rows[b] = t.kv_base + kb;  // past the segment: masked keys, finite V
+                        else
+                            rows[b] = (kb >> a.page_shift) < npages
+                                          ? a.pages[t.kv_base + (kb >> a.page_shift)] * 2 * P + (kb & (P - 1))
+                                          : -1;
+                    }
+                };
+                int rows[NB], next[NB];
+                tile_rows(0, rows);
+                for (int j = 0; j < nt; ++j) {
+                    const int s = j & 1;
+                    const uint32_t use = j >> 1;
+                    if (use > 0 && !mbar_wait(&k_empty[s], (use - 1) & 1, err, kErrWaitEmpty)) break;
+                    uint8_t *kd = sm + L::K_OFF + s * L::KV_BYTES;
+                    mbar_arrive_expect_tx(&k_full[s], L::KV_BYTES);
+#pragma unroll
+                    for (int b = 0; b < NB; ++b)
+#pragma unroll
+                        for (int h = 0; h < HALVES; ++h)
+                            tma_load_3d(kd + h * (L::KV_BYTES / HALVES) + b * R * 128, &tm_kv, &k_full[s], h * 64,
+                                        rows[b] >= 0 ? rows[b] : a.oob_row, t.kv_head);
+                    // the next tile's page ids load while this tile's V slot drains: by the
+                    // time the next K slot is free (it frees before this V slot) they are here
+                    if (j + 1 < nt) tile_rows(j + 1, next);
+                    if (use > 0 && !mbar_wait(&v_empty[s], (use - 1) & 1, err, kErrWaitEmpty)) break;
+                    uint8_t *vd = sm + L::V_OFF + s * L::KV_BYTES;
+                    mbar_arrive_expect_tx(&v_full[s], L::KV_BYTES);
+#pragma unroll
+                    for (int b = 0; b < NB; ++b)
+#pragma unroll
+                        for (int h = 0; h < HALVES; ++h)
+                            tma_load_3d(vd + h * (L::KV_BYTES / HALVES) + b * R * 128, dense ? &tm_v : &tm_kv,
+                                        &v_full[s], h * 64, rows[b] < 0 ? a.oob_row : rows[b] + (dense ? 0 : P),
+                                        t.kv_head);
+#pragma unroll
+                    for (int b = 0; b < NB; ++b) rows[b] = next[b];
+                }
+            };
+            if (lane == 0) {
+                if (dense || a.box_rows == 16)
+                    stream_tiles(IntConst<4>{});
+                else
+                    stream_tiles(IntConst<8>{});
+            }
+        } else {
+            // cp.async gather (pages of 1, 2 or 4 slots): lane e copies 16-byte chunks
+            // e, e + 32, ... of the tile's 64 K rows and 64 V rows (chunk = key * D/8 + c),
+            // writing each to its swizzled place; keys at or past the row's end read
+            // nothing and land as zeros.  The copies must have landed, and be made visible
+            // to the tensor cores' proxy, before the tile is marked full.
+            constexpr int CH = D / 8;  // 16-byte chunks per row
+            const size_t head_row = (size_t)a.num_kv_heads * D * 2;  // bytes per cache row
+            const size_t v_off = (size_t)P * head_row;
+            const uint8_t *head_base = a.kv_layer + (size_t)t.kv_head * D * 2;
             for (int j = 0; j < nt; ++j) {
                 const int s = j & 1;
                 const uint32_t use = j >> 1;
-                int rows[4];
-#pragma unroll
-                for (int pg = 0; pg < 4; ++pg) {
-                    const int pi = (kt0 + j) * 4 + pg;
-                    if (dense)
-                        rows[pg] = t.kv_base + pi * P;  // past the segment: masked keys, finite V
-                    else
-                        rows[pg] = pi < npages ? a.pages[t.kv_base + pi] * 2 * P : -1;
+                const int key0 = (kt0 + j) * kPfKeys;
+                bool ok = true;
+                if (lane == 0 && use > 0)
+                    ok = mbar_wait(&k_empty[s], (use - 1) & 1, err, kErrWaitEmpty) &&
+                         mbar_wait(&v_empty[s], (use - 1) & 1, err, kErrWaitEmpty);
+                if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+                const uint32_t kd = smem_u32(sm + L::K_OFF + s * L::KV_BYTES);
+                const uint32_t vd = smem_u32(sm + L::V_OFF + s * L::KV_BYTES);
+                for (int e = lane; e < kPfKeys * CH; e += 32) {
+                    const int key = e / CH, c = e % CH;
+                    const int pos = key0 + key;
+                    const bool valid = pos < t.length;
+                    const uint8_t *src = a.kv_layer;
+                    if (valid) {
+                        const int row = a.pages[t.kv_base + (pos >> a.page_shift)] * 2 * P + (pos & (P - 1));
+                        src = head_base + (size_t)row * head_row + c * 16;
+                    }
+                    const uint32_t dst = (c >> 3) * (L::KV_BYTES / HALVES) + swz128(key, c & 7);
+                    cp_async16(kd + dst, src, valid ? 16u : 0u);
+                    cp_async16(vd + dst, valid ? src + v_off : src, valid ? 16u : 0u);
                 }
-                if (use > 0 && !mbar_wait(&k_empty[s], (use - 1) & 1, err, kErrWaitEmpty)) break;
-                uint8_t *kd = sm + L::K_OFF + s * L::KV_BYTES;
-                mbar_arrive_expect_tx(&k_full[s], L::KV_BYTES);
-#pragma unroll
-                for (int pg = 0; pg < 4; ++pg)
-#pragma unroll
-                    for (int h = 0; h < HALVES; ++h)
-                        tma_load_3d(kd + h * (L::KV_BYTES / HALVES) + pg * 2048, &tm_kv, &k_full[s], h * 64,
-                                    rows[pg] >= 0 ? rows[pg] : a.oob_row, t.kv_head);
-                if (use > 0 && !mbar_wait(&v_empty[s], (use - 1) & 1, err, kErrWaitEmpty)) break;
-                uint8_t *vd = sm + L::V_OFF + s * L::KV_BYTES;
-                mbar_arrive_expect_tx(&v_full[s], L::KV_BYTES);
-#pragma unroll
-                for (int pg = 0; pg < 4; ++pg)
-#pragma unroll
-                    for (int h = 0; h < HALVES; ++h)
-                        tma_load_3d(vd + h * (L::KV_BYTES / HALVES) + pg * 2048, dense ? &tm_v : &tm_kv, &v_full[s],
-                                    h * 64, rows[pg] < 0 ? a.oob_row : rows[pg] + (dense ? 0 : P), t.kv_head);
+                cp_async_wait_all();
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&k_full[s]);
+                    mbar_arrive(&v_full[s]);
+                }
             }
         }
     } else if (warp == 5) {
@@ -179,7 +279,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
         constexpr uint32_t ID_O = idesc_bf16_f32(128, D, 0, 1);
         const uint32_t sQ = smem_u32(sm + L::Q_OFF);
         const uint32_t tail_begin = t.length;
-        const uint32_t tail_end = ((t.length + P - 1) / P) * P;
+        const uint32_t tail_end = (uint32_t)((t.length + P - 1) & ~(P - 1));
         bool ok = mbar_wait(q_full, 0, err, kErrWaitFull);
         auto issue_pv = [&](int i) {
             const int s = i & 1;
@@ -374,16 +474,21 @@ __global__ void __launch_bounds__(kPfThreads, 2)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 5) tmem_dealloc(tmem, kPfTmemCols);
+    if (warp == 5) tmem_dealloc(tmem, kTmemCols);
 }
 
 }  // namespace dev
 
 size_t prefill_smem_bytes(const Shape &s) {
-    // at least 100 KB, so that no more than two CTAs (2 x 256 TMEM columns) share an SM
-    const size_t need = 1024 + (s.head_dim == 64 ? dev::PfSmem<64>::BYTES : dev::PfSmem<128>::BYTES);
+    // at least 100 KB, so that no more than two CTAs (2 x 256 TMEM columns) share an SM;
+    // head_dim 256 (512 columns) takes more than half an SM's shared memory
+    const size_t need = 1024 + (s.head_dim == 64    ? dev::PfSmem<64>::BYTES
+                                : s.head_dim == 128 ? dev::PfSmem<128>::BYTES
+                                                    : dev::PfSmem<256>::BYTES);
     return need < 100 * 1024 ? 100 * 1024 : need;
 }
+static_assert(1024 + dev::PfSmem<256>::BYTES > 228 * 1024 / 2, "one head_dim-256 prefill CTA per SM");
+static_assert(1024 + dev::PfSmem<256>::BYTES <= 227 * 1024, "head_dim-256 prefill fits shared memory");
 
 template <int D, int G>
 static cudaError_t launch_prefill_t(const CUtensorMap &tkv, const CUtensorMap &tv, const CUtensorMap &tq,
@@ -396,7 +501,8 @@ static cudaError_t launch_prefill_t(const CUtensorMap &tkv, const CUtensorMap &t
 }
 
 cudaError_t launch_prefill(const Shape &s, const Plan &p, const CUtensorMap &tm_kv, const CUtensorMap &tm_v,
-                           const CUtensorMap &tm_q, void *ws, void *out, float *lse, cudaStream_t st) {
+                           const CUtensorMap &tm_q, const void *kv_layer, void *ws, void *out, float *lse,
+                           cudaStream_t st) {
     const int grid = s.graph_static ? static_counts(s, p.mode).pf_tiles : p.pf_tiles;
     if (grid == 0) return cudaSuccess;
     uint8_t *w = static_cast<uint8_t *>(ws);
@@ -406,8 +512,14 @@ cudaError_t launch_prefill(const Shape &s, const Plan &p, const CUtensorMap &tm_
     a.tiles = reinterpret_cast<const PrefillTile *>(w + p.lay.pf_tiles);
     a.pages = reinterpret_cast<const int32_t *>(w + p.lay.pf_pages);
     a.hdr = reinterpret_cast<PlanHeader *>(w + p.lay.err);
+    a.kv_layer = static_cast<const uint8_t *>(kv_layer);
     a.num_qo_heads = s.num_qo_heads;
+    a.num_kv_heads = s.num_kv_heads;
     a.page_size = s.page_size;
+    a.page_shift = s.page_shift();
+    a.box_rows = s.pf_box_rows();
+    a.gather = s.pf_gather() ? 1 : 0;
+    if (a.gather && p.mode != PKV_MODE_DENSE && !kv_layer) return cudaErrorInvalidValue;
     // a row coordinate past the tensor (TMA fills zeros); dense plans never use it
     a.oob_row = s.num_cache_pages * 2 * s.page_size;
     const size_t smem = prefill_smem_bytes(s);
@@ -415,8 +527,7 @@ cudaError_t launch_prefill(const Shape &s, const Plan &p, const CUtensorMap &tm_
     const int g = s.group();
 #define PKV_PF(DD, GG) \
     if (s.head_dim == DD && g == GG) e = launch_prefill_t<DD, GG>(tm_kv, tm_v, tm_q, a, grid, smem, st);
-    PKV_PF(64, 1) PKV_PF(64, 2) PKV_PF(64, 4) PKV_PF(64, 8) PKV_PF(64, 16)
-    PKV_PF(128, 1) PKV_PF(128, 2) PKV_PF(128, 4) PKV_PF(128, 8) PKV_PF(128, 16)
+    PKV_FOR_EACH_HEAD_DIM_AND_GROUP(PKV_PF)
 #undef PKV_PF
     return e;
 }

@@ -40,10 +40,15 @@ def _handle(**kw):
 
 @pytest.mark.parametrize("kw,status", [
     (dict(head_dim=96), B.ERR_UNSUPPORTED),
-    (dict(page_size=8), B.ERR_UNSUPPORTED),
+    (dict(head_dim=512), B.ERR_UNSUPPORTED),
+    (dict(page_size=12), B.ERR_UNSUPPORTED),
+    (dict(page_size=24), B.ERR_UNSUPPORTED),
+    (dict(page_size=48), B.ERR_UNSUPPORTED),
+    (dict(page_size=2048), B.ERR_UNSUPPORTED),
     (dict(num_qo_heads=12), B.ERR_UNSUPPORTED),
     (dict(num_qo_heads=30), B.ERR_UNSUPPORTED),
-    (dict(num_kv_heads=16, num_qo_heads=32), B.ERR_UNSUPPORTED),
+    (dict(num_kv_heads=2, num_qo_heads=24), B.ERR_UNSUPPORTED),
+    (dict(num_kv_heads=1, num_qo_heads=9), B.ERR_UNSUPPORTED),
     (dict(max_batch=0), B.ERR_INVALID),
     (dict(sink_page=200000), B.ERR_INVALID),
 ])
@@ -108,19 +113,33 @@ def test_too_many_prompt_rows_status(lib):
     assert e.value.status == B.ERR_TOO_MANY_PREFILL_ROWS
 
 
-@pytest.mark.parametrize("name,window", [("batch", -1), ("long", -1), ("long", 4096), ("tiny", -1), ("tiny", 5)])
-def test_decode_split_covers_each_visible_page_once(lib, name, window):
-    pb = wl.CONFIGS[name]()
-    h = _handle(num_qo_heads=pb.num_qo_heads, num_kv_heads=pb.num_kv_heads, head_dim=pb.head_dim,
-                num_cache_pages=pb.max_pages)
+def _split_case(name, P):
+    if P == 16:
+        return wl.CONFIGS[name]()
+    # the same lengths on pages of P slots
+    base = wl.CONFIGS[name]()
+    return wl.custom(7, base.kv_lens, base.qo_lens, num_qo_heads=base.num_qo_heads, num_kv_heads=base.num_kv_heads,
+                     head_dim=base.head_dim, page_size=P)
+
+
+@pytest.mark.parametrize("name,window,P", [("batch", -1, 16), ("long", -1, 16), ("long", 4096, 16), ("tiny", -1, 16),
+                                           ("tiny", 5, 16), ("batch", -1, 1), ("batch", -1, 8), ("long", 100, 64),
+                                           ("tiny", 5, 2)])
+@pytest.mark.parametrize("Hkv", [None, 16])
+def test_decode_split_covers_each_visible_page_once(lib, name, window, P, Hkv):
+    pb = _split_case(name, P)
+    Hkv = Hkv or pb.num_kv_heads
+    groups = 2 if Hkv == 16 else 1  # 16 kv heads: two groups of 8 share the SMs
+    h = _handle(num_qo_heads=Hkv * pb.num_qo_heads // pb.num_kv_heads, num_kv_heads=Hkv, head_dim=pb.head_dim,
+                num_cache_pages=pb.max_pages, page_size=P)
     tiles, ctas = h.decode_split(pb.kv_indptr, pb.last_page_len, window)
-    assert 1 <= ctas <= 152
+    assert 1 <= ctas <= 152 // groups
     per_cta = np.bincount(tiles[:, 4], weights=tiles[:, 2], minlength=ctas)
     assert per_cta.max() - per_cta[:-1].min() <= 1 if ctas > 1 else True
     for r in range(pb.batch):
         L = int(pb.kv_lens[r])
         lo, _ = plan_ref.visible_range(L, 1, 0, True, window)
-        want = list(range(lo // 16, (L - 1) // 16 + 1))
+        want = list(range(lo // P, (L - 1) // P + 1))
         mine = tiles[tiles[:, 0] == r]
         got = [p for t in mine for p in range(t[1], t[1] + t[2])]
         assert got == want, r
