@@ -6,8 +6,10 @@
 Default workload: batch decode, 128 requests, 32 q heads / 8 kv heads, head_dim 128,
 page_size 16, kv lengths U[512, 4096] (seed 0), a 32-layer cache
 [32, pages, 2, 16, 8, 128] bf16 of 42.7 GB.  One step = plan (host) + for each of the
-32 layer slices: last-page append, then batched decode.  The metric is KV GB/s: the K
-and V bytes of every visible token per layer, over the device time of the step.
+32 layer slices: last-page append and batched decode, in one launch
+(pkv_run_decode_append; --separate-append issues pkv_kv_append + pkv_run_decode).  The
+metric is KV GB/s: the K and V bytes of every visible token per layer, over the device
+time of the step.
 The cache streamed per step is far larger than L2, so no flush is needed.
 
 Printed: one JSON line (rank 0).  `--impl reference` times the CPU oracle on a bounded
@@ -50,6 +52,8 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-secondary", action="store_true", help="skip the prefill / mixed / long-decode lines")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--separate-append", action="store_true",
+                    help="decode workloads: pkv_kv_append + pkv_run_decode per layer instead of the fused call")
     ap.add_argument("--layers", type=int, default=0, help="fewer cache layers (profiling a small case)")
     return ap.parse_args()
 
@@ -227,26 +231,35 @@ def run_ours(args, rank, world):
     lse = torch.empty(pb.batch, pb.num_qo_heads, dtype=torch.float32, device=dev)
     kvp, kvi, lpl = pb.kv_indptr, pb.kv_indices, pb.last_page_len
     h.plan(B.MODE_DECODE, None, kvp, kvi, lpl, workspace=ws, window_left=window)
-    # launches per layer: append + decode, + the merge kernel when some cut row has more
-    # pieces than the decode kernel merges itself (4)
+    # launches per layer: the decode kernel (which also appends the layer's new tokens, or
+    # append + decode with --separate-append), + the merge kernel when some cut row has
+    # more pieces than the decode kernel merges itself (4)
     tiles, _ = h.decode_split(kvp, lpl, window)
     pieces = np.bincount(tiles[tiles[:, 3] >= 0, 0]) if (tiles[:, 3] >= 0).any() else np.zeros(1, int)
-    launches_per_layer = 2 + (1 if pieces.max() > 4 else 0)
+    launches_per_layer = (2 if args.separate_append else 1) + (1 if pieces.max() > 4 else 0)
 
     ev_pairs = []
 
-    def step(record):
+    def layer(l, q, k, v, o, ls):
+        if args.separate_append:
+            h.kv_append(k, v, cache[l], workspace=ws)
+            h.run_decode(q, cache[l], o, ls, workspace=ws)
+        else:
+            h.run_decode_append(q, k, v, cache[l], o, ls, workspace=ws)
+
+    def step(record, i=0):
+        # record: time one layer's launch per step with events on the launching stream (layer
+        # i mod L, so every layer is sampled), keeping event records out of the other gaps
         h.plan(B.MODE_DECODE, None, kvp, kvi, lpl, workspace=ws, window_left=window)
         for l in range(L):
-            h.kv_append(x["k_new"], x["v_new"], cache[l], workspace=ws)
-            if record:
+            if record and l == i % L:
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record(stream)
-                h.run_decode(x["q"], cache[l], out, lse, workspace=ws)
+                layer(l, x["q"], x["k_new"], x["v_new"], out, lse)
                 b.record(stream)
                 ev_pairs.append((a, b))
             else:
-                h.run_decode(x["q"], cache[l], out, lse, workspace=ws)
+                layer(l, x["q"], x["k_new"], x["v_new"], out, lse)
 
     for _ in range(max(args.warmup, 3)):
         step(False)
@@ -258,8 +271,8 @@ def run_ours(args, rank, world):
     torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record(stream)
-    for _ in range(args.steps):
-        step(True)
+    for i in range(args.steps):
+        step(True, i)
     t1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -286,18 +299,37 @@ def run_ours(args, rank, world):
         qh.copy_(x["q"].cpu().unsqueeze(0).expand_as(qh))
         kh.copy_(x["k_new"].cpu().unsqueeze(0).expand_as(kh))
         vh.copy_(x["v_new"].cpu().unsqueeze(0).expand_as(vh))
-        qd, kd, vd = torch.empty_like(x["q"]), torch.empty_like(x["k_new"]), torch.empty_like(x["v_new"])
+        # two device staging slots per tensor; layer l's inputs are copied in on one stream
+        # while layer l-1 computes, its outputs copied out on another while layer l+1 computes
+        qd = [torch.empty_like(x["q"]) for _ in range(2)]
+        kd = [torch.empty_like(x["k_new"]) for _ in range(2)]
+        vd = [torch.empty_like(x["v_new"]) for _ in range(2)]
+        od = [torch.empty_like(out) for _ in range(2)]
+        ld = [torch.empty_like(lse) for _ in range(2)]
+        s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev_done = [torch.cuda.Event() for _ in range(2)]
+        ev_out = [torch.cuda.Event() for _ in range(2)]
 
         def e2e_step():
             h.plan(B.MODE_DECODE, None, kvp, kvi, lpl, workspace=ws, window_left=window)
             for l in range(L):
-                qd.copy_(qh[l], non_blocking=True)
-                kd.copy_(kh[l], non_blocking=True)
-                vd.copy_(vh[l], non_blocking=True)
-                h.kv_append(kd, vd, cache[l], workspace=ws)
-                h.run_decode(qd, cache[l], out, lse, workspace=ws)
-                oh[l].copy_(out, non_blocking=True)
-                lh[l].copy_(lse, non_blocking=True)
+                b = l & 1
+                s_in.wait_event(ev_done[b])  # slot b's inputs were read by layer l-2
+                with torch.cuda.stream(s_in):
+                    qd[b].copy_(qh[l], non_blocking=True)
+                    kd[b].copy_(kh[l], non_blocking=True)
+                    vd[b].copy_(vh[l], non_blocking=True)
+                ev_in[b].record(s_in)
+                stream.wait_event(ev_in[b])
+                stream.wait_event(ev_out[b])  # slot b's outputs of layer l-2 have been copied out
+                layer(l, qd[b], kd[b], vd[b], od[b], ld[b])
+                ev_done[b].record(stream)
+                s_out.wait_event(ev_done[b])
+                with torch.cuda.stream(s_out):
+                    oh[l].copy_(od[b], non_blocking=True)
+                    lh[l].copy_(ld[b], non_blocking=True)
+                ev_out[b].record(s_out)
 
         for _ in range(3):
             e2e_step()
@@ -312,7 +344,13 @@ def run_ours(args, rank, world):
         h2d = L * (x["q"].numel() + 2 * x["k_new"].numel()) * 2 + 4 * (len(kvp) + len(kvi) + len(lpl))
         d2h = L * (out.numel() * 2 + lse.numel() * 4)
         e2e = {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-               "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+               "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "copies": "pinned host buffers; per layer H2D on one stream and D2H on another, overlapped "
+                         "with the neighbouring layers' kernels (two device staging slots)"}
+        # the last step's outputs came back: spot-check them against the device results
+        torch.cuda.synchronize()
+        layer_check = L - 1
+        assert torch.equal(oh[layer_check].to(dev), od[layer_check & 1]), "e2e output copy mismatch"
         del qh, kh, vh, oh, lh
 
     # host plan cost (the pages quote ~2 us/row iterating a tensor row, 0.1 us via numpy)
@@ -330,13 +368,16 @@ def run_ours(args, rank, world):
         "config": {"workload": f"{pb.name}: {pb.batch} requests, Hq {pb.num_qo_heads} / Hkv {pb.num_kv_heads}, "
                                f"head_dim {pb.head_dim}, page_size {pb.page_size}, {L} layers, window_left {window}",
                    "kv_cache_bytes": int(cache.numel() * 2), "kv_bytes_per_step": int(step_bytes),
+                   "step": (f"plan + {L} x (pkv_kv_append + pkv_run_decode)" if args.separate_append else
+                            f"plan + {L} x pkv_run_decode_append (append fused into the decode launch)"),
                    "l2": "inputs larger than L2: every step streams the whole cache",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "e2e": e2e,
         "gpu_launches": int(args.steps * L * launches_per_layer),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
-                     "kernel": "decode_kernel (split-KV merge fused; one run_decode)",
+                     "kernel": ("decode_kernel (one run_decode)" if args.separate_append else
+                                "decode_kernel (append and split-KV merge fused; one run_decode_append)"),
                      "launch_ms": round(launch_ms, 5), "peak_source": peaks["source"]},
         "clocks": clk,
         "plan_us_per_row": round(plan_us_row, 3),

@@ -181,6 +181,16 @@ pkv_status pkv_run_decode(pkv_handle_t h, const void *q, const void *kv_layer, v
                           void *workspace, pkv_stream_t stream);
 
 /*
+ * pkv_kv_append followed by pkv_run_decode, in one kernel launch (same results, the
+ * appended slots bit-identical).  Decode plans only (PKV_ERR_NOT_PLANNED otherwise).
+ * k, v: device bf16 [batch, num_kv_heads, head_dim], 16-byte aligned; the rest as
+ * pkv_run_decode.  The CTA that reads a row's last page writes the row's new token
+ * into it and uses it from shared memory, so no other launch orders the two.
+ */
+pkv_status pkv_run_decode_append(pkv_handle_t h, const void *q, const void *k, const void *v, void *kv_layer,
+                                 void *out, float *lse, void *workspace, pkv_stream_t stream);
+
+/*
  * Ragged prefill over a cached prefix (FlashInferPrefillWrapper.run).  q, out: device
  * bf16 [T, Hq, D] in qo_indptr order; lse: device fp32 [T, Hq] or NULL.
  */

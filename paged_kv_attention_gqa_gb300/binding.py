@@ -24,7 +24,7 @@ STATUS_NAMES = ["OK", "INVALID", "UNSUPPORTED", "WORKSPACE", "TOO_MANY_PREFILL_R
 EXPORTS = ["pkv_create", "pkv_destroy", "pkv_last_error", "pkv_workspace_size", "pkv_plan", "pkv_kv_append",
            "pkv_run_decode", "pkv_run_prefill", "pkv_run_mixed", "pkv_check_device_error", "pkv_append_slots",
            "pkv_mixed_layout", "pkv_decode_split", "pkv_run_decode_static", "pkv_context_only_views",
-           "pkv_plan_dense", "pkv_run_dense", "pkv_gather_kv"]
+           "pkv_plan_dense", "pkv_run_dense", "pkv_gather_kv", "pkv_run_decode_append"]
 
 
 class PkvError(RuntimeError):
@@ -60,6 +60,7 @@ def load(path: str = LIB_PATH):
         "pkv_plan": ([vp, i, i32p, i32p, i32p, i32p, i, i, i, ctypes.c_float, vp, ctypes.c_size_t, vp], i),
         "pkv_kv_append": ([vp, vp, vp, vp, vp, vp], i),
         "pkv_run_decode": ([vp, vp, vp, vp, vp, vp, vp], i),
+        "pkv_run_decode_append": ([vp, vp, vp, vp, vp, vp, vp, vp, vp], i),
         "pkv_run_prefill": ([vp, vp, vp, vp, vp, vp, vp], i),
         "pkv_run_mixed": ([vp, vp, vp, vp, vp, vp, vp], i),
         "pkv_check_device_error": ([vp, vp, vp, ctypes.POINTER(i)], i),
@@ -159,6 +160,11 @@ class Handle:
 
     def run_decode(self, q, kv_layer, out, lse=None, *, workspace, stream=None):
         self._run(self.lib.pkv_run_decode, q, kv_layer, out, lse, workspace, stream)
+
+    def run_decode_append(self, q, k, v, kv_layer, out, lse=None, *, workspace, stream=None):
+        """kv_append + run_decode in one launch (decode plans)."""
+        self._check(self.lib.pkv_run_decode_append(self.h, _dptr(q), _dptr(k), _dptr(v), _dptr(kv_layer), _dptr(out),
+                                                    _dptr(lse), _dptr(workspace), _stream(stream)))
 
     def run_prefill(self, q, kv_layer, out, lse=None, *, workspace, stream=None):
         self._run(self.lib.pkv_run_prefill, q, kv_layer, out, lse, workspace, stream)

@@ -45,6 +45,12 @@ struct DecodeArgs {
     float *part_lse;
     MergeRow *merges;
     PlanHeader *hdr;  // per-plan values (error word, sm_scale) in the workspace
+    // fused append (null when the plan's tokens were appended by append_kernel): the new
+    // tokens' K / V rows, the layer slice and each token's slot row in it
+    const uint4 *k_new;
+    const uint4 *v_new;
+    uint4 *kv_layer;
+    const int32_t *append_rows;
     int num_qo_heads;
     int num_kv_heads;
     int heads;         // kv heads per CTA; blockIdx.y selects the group
@@ -259,6 +265,25 @@ __global__ void __launch_bounds__((D > 128 ? 4 : 8) * 32 + 32, 1)
             const uint32_t sbase = smem_u32(st);
             const int pos0 = cr.base + k * kDecodeKeysPerStage;
             const int nvalid = cr.end - pos0;  // keys of this chunk inside the piece
+            // fused append: the row's new token (position L-1, in this piece's last chunk)
+            // replaces the slot's stale rows in the stage and is stored to the cache; only
+            // this CTA reads this head of that page, and its TMA read came first
+            const bool patch = a.k_new && t.append_token >= 0 && t.length - 1 - pos0 < kDecodeKeysPerStage;
+            if (patch) {
+                constexpr int CH = D / 8;  // 16-byte chunks per row
+                const int tok = t.length - 1 - pos0;
+                const size_t src = ((size_t)t.append_token * a.num_kv_heads + hkg) * CH;
+                const size_t row = (size_t)a.append_rows[t.append_token];
+                for (int i = lane; i < 2 * CH; i += 32) {
+                    const int kv = i / CH, c = i % CH;
+                    const uint4 val = (kv ? a.v_new : a.k_new)[src + c];
+                    const RowAddr r = key_row(a, hk, tok, kv ? vrow : 0);
+                    *reinterpret_cast<uint4 *>(st + (kv ? v_region : 0u) + (c >> 3) * half_stride + r.off +
+                                               (((c & 7) ^ r.phase) << 4)) = val;
+                    a.kv_layer[((row + (kv ? P : 0)) * a.num_kv_heads + hkg) * CH + c] = val;
+                }
+                __syncwarp();
+            }
             if (nvalid < kDecodeKeysPerStage) {
                 // zero this head's V rows past the piece's end (stale, unloaded or poisoned)
                 const int nz = (kDecodeKeysPerStage - nvalid) * (D / 8);
@@ -340,7 +365,7 @@ __global__ void __launch_bounds__((D > 128 ? 4 : 8) * 32 + 32, 1)
                 mma_bf16_16816(acc[2 * dj], pa, b0, b1);
                 mma_bf16_16816(acc[2 * dj + 1], pa, b2, b3);
             }
-            if (nvalid < kDecodeKeysPerStage) fence_proxy_async_smem();
+            if (nvalid < kDecodeKeysPerStage || patch) fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
         }
@@ -528,7 +553,7 @@ static cudaError_t launch_decode_t(const CUtensorMap &tm, const dev::DecodeArgs 
 }
 
 cudaError_t launch_decode(const Shape &s, const Plan &p, const CUtensorMap &tm, void *ws, const void *q, void *out,
-                          float *lse, cudaStream_t st) {
+                          float *lse, cudaStream_t st, const void *k_new, const void *v_new, void *kv_layer) {
     const StaticCounts sc = static_counts(s, p.mode);
     const int grid = s.graph_static ? sc.dec_ctas : p.dec_ctas;
     if (grid == 0) return cudaSuccess;
@@ -544,6 +569,10 @@ cudaError_t launch_decode(const Shape &s, const Plan &p, const CUtensorMap &tm, 
     a.part_lse = reinterpret_cast<float *>(w + p.lay.part_lse);
     a.merges = reinterpret_cast<MergeRow *>(w + p.lay.merge_rows);
     a.hdr = reinterpret_cast<PlanHeader *>(w + p.lay.err);
+    a.k_new = static_cast<const uint4 *>(k_new);
+    a.v_new = static_cast<const uint4 *>(v_new);
+    a.kv_layer = static_cast<uint4 *>(kv_layer);
+    a.append_rows = reinterpret_cast<const int32_t *>(w + p.lay.append_rows);
     a.num_qo_heads = s.num_qo_heads;
     a.num_kv_heads = s.num_kv_heads;
     a.heads = s.dec_heads();

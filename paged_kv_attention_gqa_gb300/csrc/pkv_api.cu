@@ -308,6 +308,22 @@ extern "C" pkv_status pkv_run_decode(pkv_handle_t h, const void *q, const void *
     return e == cudaSuccess ? PKV_OK : cuda_fail(h, e, "decode launch");
 }
 
+extern "C" pkv_status pkv_run_decode_append(pkv_handle_t h, const void *q, const void *k, const void *v,
+                                            void *kv_layer, void *out, float *lse, void *workspace,
+                                            pkv_stream_t stream) {
+    pkv_status st = check_planned(h, workspace, PKV_MODE_DECODE);
+    if (st != PKV_OK) return st;
+    if (h->plan.batch == 0) return PKV_OK;
+    if ((st = check_io(h, q, kv_layer, out)) != PKV_OK) return st;
+    if (!k || !v) return fail(h, PKV_ERR_INVALID, "null k or v");
+    if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(kv_layer)) % 16)
+        return fail(h, PKV_ERR_INVALID, "k, v and kv_layer must be 16-byte aligned");
+    if ((st = dec_map(h, kv_layer)) != PKV_OK) return st;
+    cudaError_t e = pkv::launch_decode(h->shape, h->plan, h->tm_dec, workspace, q, out, lse,
+                                       static_cast<cudaStream_t>(stream), k, v, kv_layer);
+    return e == cudaSuccess ? PKV_OK : cuda_fail(h, e, "decode + append launch");
+}
+
 extern "C" pkv_status pkv_run_prefill(pkv_handle_t h, const void *q, const void *kv_layer, void *out, float *lse,
                                       void *workspace, pkv_stream_t stream) {
     pkv_status st = check_planned(h, workspace, PKV_MODE_PREFILL);

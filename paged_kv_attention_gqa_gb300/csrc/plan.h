@@ -56,7 +56,8 @@ struct DecodeTile {
     int32_t lo;          // first visible position
     int32_t partial;     // split-KV partial slot, -1 = this piece is the whole row
     int32_t merge_row;   // the row's MergeRow when it is cut, else -1
-    int32_t pad[3];
+    int32_t append_token;  // fused append: the row's new token (last piece only), else -1
+    int32_t pad[2];
 };
 static_assert(sizeof(DecodeTile) == 48, "DecodeTile is 12 ints");
 
@@ -184,7 +185,7 @@ int mixed_layout(const int32_t *qo, const int32_t *kvp, const int32_t *kvi, cons
 void decode_split(const Shape &s, int rows, const int32_t *kvp, const int32_t *lpl, const int32_t *q_token,
                   const int32_t *out_token, int window_left, std::vector<DecodeTile> &tiles,
                   std::vector<int32_t> &cta_ptr, std::vector<MergeRow> &merges, int &num_partials,
-                  int max_ctas = 0);
+                  int max_ctas = 0, bool mark_append = false);
 int decode_cta_limit(const Shape &s);
 // Dense varlen plan (mstar.engine.resources.attn.dense, DensePlan): segment r's queries are
 // q[cu_q[r]..cu_q[r+1]), its keys rows cu_k[r]..cu_k[r+1] of contiguous K / V.

@@ -216,7 +216,8 @@ static constexpr int kMinKeysPerCta = 32;
 
 void decode_split(const Shape &s, int rows, const int32_t *kvp, const int32_t *lpl, const int32_t *q_token,
                   const int32_t *out_token, int window_left, std::vector<DecodeTile> &tiles,
-                  std::vector<int32_t> &cta_ptr, std::vector<MergeRow> &merges, int &num_partials, int max_ctas) {
+                  std::vector<int32_t> &cta_ptr, std::vector<MergeRow> &merges, int &num_partials, int max_ctas,
+                  bool mark_append) {
     const int P = s.page_size;
     tiles.clear();
     cta_ptr.assign(1, 0);
@@ -257,7 +258,8 @@ void decode_split(const Shape &s, int rows, const int32_t *kvp, const int32_t *l
                 t.lo = lo[r];
                 t.partial = -1;
                 t.merge_row = -1;
-                t.pad[0] = t.pad[1] = t.pad[2] = 0;
+                t.append_token = -1;
+                t.pad[0] = t.pad[1] = 0;
                 row_tiles[r].push_back((int)tiles.size());
                 tiles.push_back(t);
                 used += take;
@@ -270,6 +272,11 @@ void decode_split(const Shape &s, int rows, const int32_t *kvp, const int32_t *l
         }
         cta_ptr.push_back((int32_t)tiles.size());
     }
+    // the piece holding a row's last position also stores its new token (decode plans:
+    // the row's only token, the one its query comes from)
+    if (mark_append)
+        for (int rr = 0; rr < rows; ++rr)
+            if (!row_tiles[rr].empty()) tiles[row_tiles[rr].back()].append_token = q_token[rr];
     for (int rr = 0; rr < rows; ++rr) {
         if (row_tiles[rr].size() <= 1) continue;
         MergeRow m;
@@ -524,7 +531,8 @@ int make_plan(const Shape &s, int mode, const int32_t *qo, const int32_t *kvp, c
     if (mode == PKV_MODE_DECODE) {
         std::vector<int32_t> qt(batch), ot(batch);
         for (int r = 0; r < batch; ++r) qt[r] = ot[r] = r;
-        decode_split(s, batch, kvp, lpl, qt.data(), ot.data(), window_left, dtiles, cta_ptr, merges, partials);
+        decode_split(s, batch, kvp, lpl, qt.data(), ot.data(), window_left, dtiles, cta_ptr, merges, partials, 0,
+                     plan.num_append > 0);
         dec_pages.assign(kvi, kvi + kvp[batch]);
         plan.dec_rows = batch;
     } else if (mode == PKV_MODE_PREFILL) {

@@ -28,8 +28,9 @@ def make_handle(pb, *, sm_count=0, max_prefill_rows=None):
 
 
 def gpu_step(pb, x, mode, *, layer=0, window_left=-1, causal=True, sm_scale=0.0, sm_count=0, append=True,
-             handle=None, workspace=None):
-    """plan -> append -> run for one layer; returns (out, lse, handle, workspace)."""
+             handle=None, workspace=None, fused=False):
+    """plan -> append -> run for one layer; returns (out, lse, handle, workspace).  fused:
+    decode plans append inside the decode launch (pkv_run_decode_append)."""
     h = handle or make_handle(pb, sm_count=sm_count)
     m = MODES[mode]
     ws = workspace if workspace is not None else torch.empty(h.workspace_size(m), dtype=torch.uint8, device="cuda")
@@ -37,12 +38,16 @@ def gpu_step(pb, x, mode, *, layer=0, window_left=-1, causal=True, sm_scale=0.0,
     h.plan(m, qo, pb.kv_indptr, pb.kv_indices, pb.last_page_len, workspace=ws, causal=causal,
            window_left=window_left, sm_scale=sm_scale)
     kv = x["kv_cache"][layer]
-    if append and x.get("k_new") is not None:
-        h.kv_append(x["k_new"], x["v_new"], kv, workspace=ws)
     q = x["q"]
     out = torch.full_like(q, float("nan"))
     lse = torch.full((q.shape[0], q.shape[1]), float("nan"), dtype=torch.float32, device="cuda")
-    getattr(h, "run_" + mode)(q, kv, out, lse, workspace=ws)
+    if fused:
+        assert mode == "decode" and append
+        h.run_decode_append(q, x["k_new"], x["v_new"], kv, out, lse, workspace=ws)
+    else:
+        if append and x.get("k_new") is not None:
+            h.kv_append(x["k_new"], x["v_new"], kv, workspace=ws)
+        getattr(h, "run_" + mode)(q, kv, out, lse, workspace=ws)
     torch.cuda.synchronize()
     assert h.check_device_error(ws) == 0
     return out, lse, h, ws

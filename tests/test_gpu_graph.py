@@ -106,3 +106,56 @@ def test_captured_step_replays_after_replanning(mode):
         T = pb.num_tokens
         ref_o, ref_l = G.oracle_attn(pb, wl.bf16_bits(x["q"]), after)
         G.compare(out[:T], lse[:T], ref_o, ref_l, what=f"{mode} replay {i}")
+
+
+def test_captured_fused_decode_append_replays_after_replanning():
+    """pkv_run_decode_append (one launch) captured once, replayed after new decode plans."""
+    from paged_kv_attention_gqa_gb300 import build
+    build.build()
+    steps = _steps("decode")
+    max_batch = 8
+    n_pages = steps[0].max_pages
+    h = B.Handle(num_qo_heads=HQ, num_kv_heads=HKV, head_dim=D, page_size=16, max_batch=max_batch,
+                 max_total_tokens=max_batch, max_num_pages=POOL, num_cache_pages=n_pages, max_prefill_rows=0,
+                 graph_static=1)
+    ws = torch.empty(h.workspace_size(B.MODE_DECODE), dtype=torch.uint8, device="cuda")
+    q = torch.zeros(max_batch, HQ, D, dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros(max_batch, HKV, D, dtype=torch.bfloat16, device="cuda")
+    v = torch.zeros_like(k)
+    out = torch.zeros_like(q)
+    lse = torch.zeros(max_batch, HQ, dtype=torch.float32, device="cuda")
+    kv = torch.zeros(n_pages, 2, 16, HKV, D, dtype=torch.bfloat16, device="cuda")
+
+    def load(pb, seed):
+        x = wl.make_inputs(pb, device="cuda", seed=seed, unused="nan", layers=1)
+        T = pb.num_tokens
+        q[:T].copy_(x["q"])
+        k[:T].copy_(x["k_new"])
+        v[:T].copy_(x["v_new"])
+        kv.copy_(x["kv_cache"][0])
+        return x
+
+    def plan(pb):
+        h.plan(B.MODE_DECODE, None, pb.kv_indptr, pb.kv_indices, pb.last_page_len, workspace=ws)
+
+    load(steps[0], 0)
+    plan(steps[0])
+    h.run_decode_append(q, k, v, kv, out, lse, workspace=ws)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        h.run_decode_append(q, k, v, kv, out, lse, workspace=ws)
+    torch.cuda.synchronize()
+    for i, pb in enumerate(steps[::-1] + steps[:1]):
+        x = load(pb, 30 + i)
+        before = wl.bf16_bits(kv)
+        out.fill_(float("nan"))
+        plan(pb)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert h.check_device_error(ws) == 0
+        after = G.oracle_append(pb, before, x)
+        assert np.array_equal(wl.bf16_bits(kv), after), f"replay {i}: appended cache differs"
+        T = pb.num_tokens
+        ref_o, ref_l = G.oracle_attn(pb, wl.bf16_bits(x["q"]), after)
+        G.compare(out[:T], lse[:T], ref_o, ref_l, what=f"fused replay {i}")

@@ -27,11 +27,11 @@ def _build():
 
 
 def _check_step(pb, mode, *, window_left=-1, causal=True, sm_scale=0.0, sm_count=0, seed=0, unused="nan",
-                rows=None):
+                rows=None, fused=False):
     x = wl.make_inputs(pb, device="cuda", seed=seed, unused=unused, layers=1)
     before = wl.bf16_bits(x["kv_cache"][0])
     out, lse, h, ws = G.gpu_step(pb, x, mode, window_left=window_left, causal=causal, sm_scale=sm_scale,
-                                 sm_count=sm_count)
+                                 sm_count=sm_count, fused=fused)
     after = G.oracle_append(pb, before, x)
     got = wl.bf16_bits(x["kv_cache"][0])
     assert np.array_equal(got, after), "appended cache differs from the oracle's (bit-exact)"
@@ -69,6 +69,39 @@ def test_decode_forced_splits(sm_count):
     lens = [700, 33, 1, 2048, 129, 16, 4000]
     pb = wl.custom(5, lens, [1] * len(lens), num_qo_heads=64, num_kv_heads=8, head_dim=128, page_size=16)
     _check_step(pb, "decode", sm_count=sm_count, seed=3)
+
+
+# ------------------------------------------------------------------ append fused into the decode launch
+
+@pytest.mark.parametrize("D,Hq,Hkv", [(128, 32, 8), (64, 8, 2), (128, 16, 1)])
+@pytest.mark.parametrize("sm_count", [0, 1, 3, 7, 300])
+def test_decode_append_fused(D, Hq, Hkv, sm_count):
+    """pkv_run_decode_append: the appended slice bit-exact and the outputs at tolerance,
+    with the row's new token taken from the stage patched in shared memory (poisoned
+    slots would show otherwise: the slot holds NaN until the append)."""
+    lens = [1, 2, 15, 16, 17, 31, 32, 33, 100, 257, 1000, 4000]
+    pb = wl.custom(20, lens, [1] * len(lens), num_qo_heads=Hq, num_kv_heads=Hkv, head_dim=D, page_size=16)
+    _check_step(pb, "decode", sm_count=sm_count, seed=21, fused=True)
+
+
+@pytest.mark.parametrize("window", [0, 1, 16, 100])
+def test_decode_append_fused_window(window):
+    lens = [1, 5, 16, 17, 40, 300, 1500]
+    pb = wl.custom(22, lens, [1] * len(lens), num_qo_heads=32, num_kv_heads=8, head_dim=128, page_size=16)
+    _check_step(pb, "decode", window_left=window, seed=23, fused=True)
+
+
+def test_decode_append_fused_equals_separate_calls():
+    """Same plan, same inputs: the fused launch gives the same bits as append + decode."""
+    lens = [700, 33, 1, 2048, 129, 16, 4000]
+    pb = wl.custom(24, lens, [1] * len(lens), num_qo_heads=32, num_kv_heads=8, head_dim=128, page_size=16)
+    res = []
+    for fused in (False, True):
+        x = wl.make_inputs(pb, device="cuda", seed=25, unused="nan", layers=1)
+        out, lse, _, _ = G.gpu_step(pb, x, "decode", fused=fused)
+        res.append((wl.bf16_bits(out), lse.cpu().numpy(), wl.bf16_bits(x["kv_cache"][0])))
+    for a, b in zip(*res):
+        assert np.array_equal(a, b)
 
 
 def test_decode_sm_scale():

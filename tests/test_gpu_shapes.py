@@ -25,10 +25,11 @@ def _build():
     build.build()
 
 
-def _check_step(pb, mode, *, window_left=-1, causal=True, sm_count=0, seed=0):
+def _check_step(pb, mode, *, window_left=-1, causal=True, sm_count=0, seed=0, fused=False):
     x = wl.make_inputs(pb, device="cuda", seed=seed, unused="nan", layers=1)
     before = wl.bf16_bits(x["kv_cache"][0])
-    out, lse, h, ws = G.gpu_step(pb, x, mode, window_left=window_left, causal=causal, sm_count=sm_count)
+    out, lse, h, ws = G.gpu_step(pb, x, mode, window_left=window_left, causal=causal, sm_count=sm_count,
+                                 fused=fused)
     after = G.oracle_append(pb, before, x)
     assert np.array_equal(wl.bf16_bits(x["kv_cache"][0]), after), "appended cache differs (bit-exact)"
     ref_o, ref_l = G.oracle_attn(pb, wl.bf16_bits(x["q"]), after, causal=causal if mode != "decode" else True,
@@ -54,6 +55,17 @@ def test_decode_page_sizes(P, Hq, Hkv, D):
     pb = wl.custom(100 + P, lens, [1] * len(lens), num_qo_heads=Hq, num_kv_heads=Hkv, head_dim=D, page_size=P,
                    pool_factor=1.3)
     _check_step(pb, "decode", seed=P)
+
+
+@pytest.mark.parametrize("P", PAGE_SIZES)
+@pytest.mark.parametrize("Hq,Hkv,D,sm_count", [(32, 8, 128, 0), (8, 1, 64, 5), (16, 4, 256, 0), (32, 16, 128, 10)])
+def test_decode_append_fused_page_sizes(P, Hq, Hkv, D, sm_count):
+    """The fused append patches the new token's slot wherever the page layout puts it
+    (K and V in separate boxes, or one box per page below 8 slots; head groups)."""
+    lens = _decode_lens(P)
+    pb = wl.custom(250 + P, lens, [1] * len(lens), num_qo_heads=Hq, num_kv_heads=Hkv, head_dim=D, page_size=P,
+                   pool_factor=1.3)
+    _check_step(pb, "decode", sm_count=sm_count, seed=P + 7, fused=True)
 
 
 @pytest.mark.parametrize("P", PAGE_SIZES)
