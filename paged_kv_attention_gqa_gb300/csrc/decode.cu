@@ -168,13 +168,15 @@ __global__ void __launch_bounds__((D > 128 ? 4 : 8) * 32 + 32, 1)
             mbar_init(&empty[s], Hc);
         }
         fence_barrier_init();
+        prefetch_tmap(&tmap);
     }
     __syncthreads();
+    griddep_wait();  // inputs, the cache and the merge counters may come from the previous kernel
+    griddep_launch();
 
     if (warp == Hc) {
         // ---------------- producer ----------------
         if (lane == 0) {
-            prefetch_tmap(&tmap);
             const int nkv = a.kv_in_box ? 1 : 2;
             const uint32_t box_bytes = (uint32_t)a.box_rows * Hc * 128;
             uint32_t it = 0;
@@ -442,6 +444,8 @@ constexpr int kMergeThreads = 256;
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const PlanHeader *hdr, const MergeRow *rows,
                                                               const float *part_o, const float *part_lse,
                                                               __nv_bfloat16 *out, float *lse, int Hq, int D) {
+    griddep_wait();
+    griddep_launch();
     if (hdr->fused_merge || (int)blockIdx.x >= hdr->num_merge) return;
     const MergeRow mr = rows[blockIdx.x];
     if (mr.out_token < 0) return;
@@ -474,6 +478,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const PlanHeader *
 // viewed as [pages * 2 * page_size] rows (V rows page_size further).
 __global__ void __launch_bounds__(256) append_kernel(const PlanHeader *hdr, const uint4 *k, const uint4 *v, uint4 *cache,
                                                      const int32_t *rows, int vec_per_token, int page_size) {
+    griddep_wait();
+    griddep_launch();
     const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     const int t = (int)(i / vec_per_token), c = (int)(i % vec_per_token);
     if (t >= hdr->num_append) return;
@@ -488,6 +494,8 @@ __global__ void __launch_bounds__(256) append_kernel(const PlanHeader *hdr, cons
 // K and V of slot t % page_size of page pages[t / page_size] to row t of k_out / v_out.
 __global__ void __launch_bounds__(256) gather_kernel(const uint4 *cache, const int32_t *pages, int num_tokens,
                                                      int vec_per_token, int page_size, uint4 *k_out, uint4 *v_out) {
+    griddep_wait();
+    griddep_launch();
     const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= num_tokens) return;
     const size_t row = (size_t)pages[t / page_size] * 2 * page_size + t % page_size;
@@ -512,10 +520,9 @@ cudaError_t launch_gather(const Shape &s, const void *kv_layer, const int32_t *p
     if (num_tokens <= 0) return cudaSuccess;
     const int vec = s.num_kv_heads * s.head_dim * 2 / 16;
     const int wpb = 8;
-    dev::gather_kernel<<<(num_tokens + wpb - 1) / wpb, wpb * 32, 0, st>>>(
-        static_cast<const uint4 *>(kv_layer), pages, num_tokens, vec, s.page_size, static_cast<uint4 *>(k_out),
-        static_cast<uint4 *>(v_out));
-    return cudaGetLastError();
+    return launch_pdl(dev::gather_kernel, dim3((num_tokens + wpb - 1) / wpb), dim3(wpb * 32), 0, st,
+                      static_cast<const uint4 *>(kv_layer), pages, num_tokens, vec, s.page_size,
+                      static_cast<uint4 *>(k_out), static_cast<uint4 *>(v_out));
 }
 
 static uint32_t decode_stage_bytes(const Shape &s) {
@@ -548,8 +555,7 @@ static cudaError_t launch_decode_t(const CUtensorMap &tm, const dev::DecodeArgs 
     auto fn = dev::decode_kernel<D, G>;
     cudaError_t e = set_smem_limit((const void *)fn, smem, st);
     if (e != cudaSuccess) return e;
-    fn<<<grid, warps * 32, smem, st>>>(tm, a);
-    return cudaGetLastError();
+    return launch_pdl(fn, grid, dim3(warps * 32), smem, st, tm, a);
 }
 
 cudaError_t launch_decode(const Shape &s, const Plan &p, const CUtensorMap &tm, void *ws, const void *q, void *out,
@@ -600,10 +606,10 @@ cudaError_t launch_decode(const Shape &s, const Plan &p, const CUtensorMap &tm, 
     if (merges) {
         const int heads_per_cta = dev::kMergeThreads / (s.head_dim / 4);
         const dim3 mgrid(merges, (s.num_qo_heads + heads_per_cta - 1) / heads_per_cta);
-        dev::merge_kernel<<<mgrid, dev::kMergeThreads, 0, st>>>(
-            a.hdr, reinterpret_cast<const MergeRow *>(w + p.lay.merge_rows), a.part_o, a.part_lse, a.out, lse,
-            s.num_qo_heads, s.head_dim);
-        e = cudaGetLastError();
+        e = launch_pdl(dev::merge_kernel, mgrid, dim3(dev::kMergeThreads), 0, st,
+                       static_cast<const PlanHeader *>(a.hdr), reinterpret_cast<const MergeRow *>(w + p.lay.merge_rows),
+                       static_cast<const float *>(a.part_o), static_cast<const float *>(a.part_lse), a.out, lse,
+                       s.num_qo_heads, s.head_dim);
     }
     return e;
 }
@@ -616,11 +622,10 @@ cudaError_t launch_append(const Shape &s, const Plan &p, void *ws, const void *k
     const int vec = s.num_kv_heads * s.head_dim * 2 / 16;
     const long long chunks = (long long)tokens * vec;
     const int grid = (int)((chunks + 255) / 256);
-    dev::append_kernel<<<grid, 256, 0, st>>>(
-        reinterpret_cast<const PlanHeader *>(w + p.lay.err), static_cast<const uint4 *>(k),
-        static_cast<const uint4 *>(v), static_cast<uint4 *>(kv_layer),
-        reinterpret_cast<const int32_t *>(w + p.lay.append_rows), vec, s.page_size);
-    return cudaGetLastError();
+    return launch_pdl(dev::append_kernel, dim3(grid), dim3(256), 0, st,
+                      reinterpret_cast<const PlanHeader *>(w + p.lay.err), static_cast<const uint4 *>(k),
+                      static_cast<const uint4 *>(v), static_cast<uint4 *>(kv_layer),
+                      reinterpret_cast<const int32_t *>(w + p.lay.append_rows), vec, s.page_size);
 }
 
 }  // namespace pkv

@@ -3,6 +3,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <utility>
+
 #include "plan.h"
 
 // Every (head_dim, group size) the kernels are compiled for.
@@ -10,6 +12,25 @@
 #define PKV_FOR_EACH_HEAD_DIM_AND_GROUP(X) PKV_FOR_EACH_GROUP(X, 64) PKV_FOR_EACH_GROUP(X, 128) PKV_FOR_EACH_GROUP(X, 256)
 
 namespace pkv {
+
+// Launch `kernel` with programmatic stream serialization (see griddep_wait in ptx.cuh):
+// every kernel of this library waits for its predecessor on the stream in-kernel, after
+// its prologue, so the launch itself may overlap the predecessor's tail.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 int decode_stages(const Shape &s);
 cudaError_t set_smem_limit(const void *fn, size_t smem, cudaStream_t st);

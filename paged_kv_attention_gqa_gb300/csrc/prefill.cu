@@ -145,6 +145,8 @@ __global__ void __launch_bounds__(kPfThreads, D > 128 ? 1 : 2)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    griddep_wait();  // q, the cache (or K / V) may come from the previous kernel
+    griddep_launch();
     const uint32_t tmem = *tmem_holder;
     const uint32_t S_col[2] = {tmem, tmem + 64};
     const uint32_t O_col = tmem + 128;
@@ -496,8 +498,7 @@ static cudaError_t launch_prefill_t(const CUtensorMap &tkv, const CUtensorMap &t
     auto fn = dev::prefill_tc_kernel<D, G>;
     cudaError_t e = set_smem_limit((const void *)fn, smem, st);
     if (e != cudaSuccess) return e;
-    fn<<<grid, dev::kPfThreads, smem, st>>>(tkv, tv, tq, a);
-    return cudaGetLastError();
+    return launch_pdl(fn, dim3(grid), dim3(dev::kPfThreads), smem, st, tkv, tv, tq, a);
 }
 
 cudaError_t launch_prefill(const Shape &s, const Plan &p, const CUtensorMap &tm_kv, const CUtensorMap &tm_v,

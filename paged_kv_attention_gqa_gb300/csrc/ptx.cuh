@@ -75,6 +75,15 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, uint64_
         : "memory");
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may start while the previous kernel on its stream is still running:
+// griddep_wait() blocks until that kernel has completed and its memory is visible (a
+// no-op for an ordinary launch), so nothing it writes is read before.  griddep_launch()
+// lets the next such kernel on the stream be scheduled now; it still waits for this
+// one in its own griddep_wait().
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // 16-byte global -> shared copy (L2 only); src_bytes = 0 writes 16 zero bytes and reads
 // nothing.
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
