@@ -437,39 +437,70 @@ __global__ void __launch_bounds__((D > 128 ? 4 : 8) * 32 + 32, 1)
 
 // Merge the split-KV partials of each cut row when the plan does not fuse merges into the
 // decode kernel: with w_j = exp(lse_j - max lse), o = sum_j w_j o_j / sum_j w_j and
-// lse = max lse + ln sum_j w_j.  Grid: (cut rows, head groups of 1024 / D heads); one
-// thread per (head, 4 columns), 256 threads.
+// lse = max lse + ln sum_j w_j.  One CTA per (cut row, q head), 256 threads: one warp
+// reduces the row's lse values to the max and the weight sum; then thread (slot, c) sums
+// pieces slot, slot + S, ... (S = 256 / (D/4) slots) for 4 columns c, so every partial of
+// the row is in flight at once, and the slots are added through shared memory.
 constexpr int kMergeThreads = 256;
 
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const PlanHeader *hdr, const MergeRow *rows,
                                                               const float *part_o, const float *part_lse,
                                                               __nv_bfloat16 *out, float *lse, int Hq, int D) {
+    __shared__ float4 s_acc[kMergeThreads];
+    __shared__ float s_red[2];
     griddep_wait();
     griddep_launch();
     if (hdr->fused_merge || (int)blockIdx.x >= hdr->num_merge) return;
     const MergeRow mr = rows[blockIdx.x];
     if (mr.out_token < 0) return;
-    const int per_head = D / 4;
-    const int h = blockIdx.y * (kMergeThreads / per_head) + threadIdx.x / per_head;
-    const int c = (threadIdx.x % per_head) * 4;
-    if (h >= Hq) return;
-    float M = -INFINITY;
-    for (int j = 0; j < mr.count; ++j) M = fmaxf(M, part_lse[(size_t)(mr.first + j) * Hq + h]);
-    float wsum = 0.f;
+    const int h = blockIdx.y;
+    const int count = mr.count;
+    const float *lse_of = part_lse + (size_t)mr.first * Hq + h;  // piece j at lse_of[j * Hq]
+    if (threadIdx.x < 32) {
+        float M = -INFINITY;
+        for (int j = threadIdx.x; j < count; j += 32) M = fmaxf(M, __ldcg(lse_of + (size_t)j * Hq));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        float sum = 0.f;
+        for (int j = threadIdx.x; j < count; j += 32) sum += __expf(__ldcg(lse_of + (size_t)j * Hq) - M);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        if (threadIdx.x == 0) {
+            s_red[0] = M;
+            s_red[1] = sum;
+        }
+    }
+    __syncthreads();
+    const float M = s_red[0];
+    // weighted partial sums: slot = threadIdx / (D/4), 4 columns each
+    const int per_piece = D / 4;
+    const int slots = kMergeThreads / per_piece;
+    const int slot = threadIdx.x / per_piece, c = (threadIdx.x % per_piece) * 4;
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = 0; j < mr.count; ++j) {
-        const float w = __expf(part_lse[(size_t)(mr.first + j) * Hq + h] - M);
-        const float4 v = *reinterpret_cast<const float4 *>(part_o + ((size_t)(mr.first + j) * Hq + h) * D + c);
-        wsum += w;
+#pragma unroll 4
+    for (int j = slot; j < count; j += slots) {
+        const float w = __expf(__ldcg(lse_of + (size_t)j * Hq) - M);
+        const float4 v = __ldcg(reinterpret_cast<const float4 *>(part_o + ((size_t)(mr.first + j) * Hq + h) * D + c));
         o.x += w * v.x;
         o.y += w * v.y;
         o.z += w * v.z;
         o.w += w * v.w;
     }
-    const float inv = 1.f / wsum;
-    __nv_bfloat16 *dst = out + ((size_t)mr.out_token * Hq + h) * D + c;
-    *reinterpret_cast<uint2 *>(dst) = make_uint2(pack_bf16(o.x * inv, o.y * inv), pack_bf16(o.z * inv, o.w * inv));
-    if (lse && c == 0) lse[(size_t)mr.out_token * Hq + h] = M + __logf(wsum);
+    s_acc[threadIdx.x] = o;
+    __syncthreads();
+    if (slot == 0) {
+        for (int k = 1; k < slots; ++k) {
+            const float4 v = s_acc[k * per_piece + threadIdx.x];
+            o.x += v.x;
+            o.y += v.y;
+            o.z += v.z;
+            o.w += v.w;
+        }
+        const float inv = 1.f / s_red[1];
+        __nv_bfloat16 *dst = out + ((size_t)mr.out_token * Hq + h) * D + c;
+        *reinterpret_cast<uint2 *>(dst) = make_uint2(pack_bf16(o.x * inv, o.y * inv), pack_bf16(o.z * inv, o.w * inv));
+        if (lse && c == 0) lse[(size_t)mr.out_token * Hq + h] = M + __logf(s_red[1]);
+    }
 }
 
 
@@ -604,8 +635,7 @@ cudaError_t launch_decode(const Shape &s, const Plan &p, const CUtensorMap &tm, 
     // and it returns at once when the plan merged inside the decode kernel)
     const int merges = s.graph_static ? sc.num_merge : (p.fused_merge ? 0 : p.num_merge);
     if (merges) {
-        const int heads_per_cta = dev::kMergeThreads / (s.head_dim / 4);
-        const dim3 mgrid(merges, (s.num_qo_heads + heads_per_cta - 1) / heads_per_cta);
+        const dim3 mgrid(merges, s.num_qo_heads);
         e = launch_pdl(dev::merge_kernel, mgrid, dim3(dev::kMergeThreads), 0, st,
                        static_cast<const PlanHeader *>(a.hdr), reinterpret_cast<const MergeRow *>(w + p.lay.merge_rows),
                        static_cast<const float *>(a.part_o), static_cast<const float *>(a.part_lse), a.out, lse,
