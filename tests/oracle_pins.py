@@ -147,6 +147,9 @@ SDPA_CASES = [
     ([40, 21, 64], [9, 21, 3], 16, 2, 16, 16, False, -1),
     ([70, 3], [70, 2], 8, 1, 8, 8, True, 17),
     ([29, 31], [1, 1], 4, 4, 16, 1, True, 0),
+    ([130, 9], [3, 1], 14, 2, 256, 2, True, -1),       # head_dim 256, group 7, 2-slot pages
+    ([200, 65], [65, 1], 6, 2, 128, 64, False, -1),    # group 3, 64-slot pages, non-causal
+    ([100, 40], [1, 40], 40, 40, 32, 32, True, 10),    # 40 kv heads, window
 ]
 
 
