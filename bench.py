@@ -557,7 +557,48 @@ def secondary(B, dev, peaks, seed):
             "frac": round(gbs / peaks["hbm_gbs"], 4)}
         del x, kv
     torch.cuda.empty_cache()
+    res["shapes"] = shape_lines(B, dev, peaks, seed, flush)
     return res
+
+
+def shape_lines(B, dev, peaks, seed, flush):
+    """The batch-decode and ragged-prefill workloads' lengths on other page sizes, head
+    dims, group sizes and kv-head counts (one layer each, per call after an L2 flush)."""
+    out = []
+    base = wl.config_batch_decode(seed=seed, num_layers=1)
+    ones = np.ones(base.batch, np.int64)
+    for P, Hq, Hkv, D in [(1, 32, 8, 128), (8, 32, 8, 128), (64, 32, 8, 128), (16, 16, 8, 256), (16, 32, 16, 128),
+                          (16, 28, 4, 128), (16, 16, 2, 128), (16, 8, 1, 128)]:
+        pb = wl.custom(seed, base.kv_lens, ones, num_qo_heads=Hq, num_kv_heads=Hkv, head_dim=D, page_size=P)
+        x = wl.make_inputs(pb, device=dev, seed=seed, unused="randn", layers=1)
+        h = make_handle(pb, B)
+        ws = torch.empty(h.workspace_size(B.MODE_DECODE), dtype=torch.uint8, device=dev)
+        h.plan(B.MODE_DECODE, None, pb.kv_indptr, pb.kv_indices, pb.last_page_len, workspace=ws)
+        kv = x["kv_cache"][0]
+        o = torch.empty_like(x["q"])
+        ls = torch.empty(x["q"].shape[:2], dtype=torch.float32, device=dev)
+        ms = time_runs(lambda: h.run_decode(x["q"], kv, o, ls, workspace=ws), flush)
+        gbs = decode_kv_bytes(pb) / (ms * 1e-3) / 1e9
+        out.append({"pass": "decode", "shape": f"P {P}, {Hq}/{Hkv}/{D}, 128 rows L U[512,4096]",
+                    "ms": round(ms, 4), "gbs": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 4)})
+        del x, kv
+    base = wl.config_prefill(seed=seed)
+    for P, Hq, Hkv, D in [(1, 32, 8, 128), (64, 32, 8, 128), (16, 16, 8, 256), (16, 28, 4, 128)]:
+        pb = wl.custom(seed, base.kv_lens, base.qo_lens, num_qo_heads=Hq, num_kv_heads=Hkv, head_dim=D, page_size=P)
+        x = wl.make_inputs(pb, device=dev, seed=seed, unused="randn", layers=1)
+        h = make_handle(pb, B)
+        ws = torch.empty(h.workspace_size(B.MODE_PREFILL), dtype=torch.uint8, device=dev)
+        h.plan(B.MODE_PREFILL, pb.qo_indptr, pb.kv_indptr, pb.kv_indices, pb.last_page_len, workspace=ws)
+        kv = x["kv_cache"][0]
+        o = torch.empty_like(x["q"])
+        ls = torch.empty(x["q"].shape[:2], dtype=torch.float32, device=dev)
+        ms = time_runs(lambda: h.run_prefill(x["q"], kv, o, ls, workspace=ws), flush)
+        tf = prefill_flops(pb) / (ms * 1e-3) / 1e12
+        out.append({"pass": "prefill", "shape": f"P {P}, {Hq}/{Hkv}/{D}, 16 rows as the ragged-prefill workload",
+                    "ms": round(ms, 4), "tflops": round(tf, 1), "frac": round(tf / peaks["bf16_tflops"], 4)})
+        del x, kv
+    torch.cuda.empty_cache()
+    return out
 
 
 def cpu_baseline(pb, seed, window, reps=1):

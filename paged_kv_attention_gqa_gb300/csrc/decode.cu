@@ -180,38 +180,73 @@ __global__ void __launch_bounds__((D > 128 ? 4 : 8) * 32 + 32, 1)
             const int nkv = a.kv_in_box ? 1 : 2;
             const uint32_t box_bytes = (uint32_t)a.box_rows * Hc * 128;
             uint32_t it = 0;
-            bool ok = true;
-            for (int ti = t_begin; ti < t_end && ok; ++ti) {
-                const DecodeTile t = a.tiles[ti];
-                const ChunkRange cr = chunk_range(t, P);
-                for (int k = cr.k0; k < cr.nk; ++k, ++it) {
-                    const int s = it % a.stages;
-                    const uint32_t use = it / a.stages;
-                    if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, err, kErrWaitEmpty)) {
-                        ok = false;
-                        break;
-                    }
-                    const int pos0 = cr.base + k * kDecodeKeysPerStage;
-                    const int nbox = min(nb, (cr.end - pos0 + kpb - 1) / kpb);
-                    uint8_t *st = smem + (size_t)s * a.stage_bytes;
-                    mbar_arrive_expect_tx(&full[s], (uint32_t)(nbox * nkv * HALVES) * box_bytes);
-                    for (int b = 0; b < nbox; ++b) {
-                        const int pb = pos0 + b * kpb;
-                        const int page = a.pages[t.kv_base + (pb >> a.page_shift)];
-                        const int row = page * 2 * P + (pb & (P - 1));
+            if (nb == 1) {
+                // one box (of K and of V) per chunk: its page id is loaded after the slot frees
+                for (int ti = t_begin; ti < t_end; ++ti) {
+                    const DecodeTile t = a.tiles[ti];
+                    const ChunkRange cr = chunk_range(t, P);
+                    bool ok = true;
+                    for (int k = cr.k0; k < cr.nk; ++k, ++it) {
+                        const int s = it % a.stages;
+                        const uint32_t use = it / a.stages;
+                        if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, err, kErrWaitEmpty)) {
+                            ok = false;
+                            break;
+                        }
+                        const int pos0 = cr.base + k * kDecodeKeysPerStage;
+                        const int row = a.pages[t.kv_base + (pos0 >> a.page_shift)] * 2 * P + (pos0 & (P - 1));
+                        uint8_t *st = smem + (size_t)s * a.stage_bytes;
+                        mbar_arrive_expect_tx(&full[s], (uint32_t)(nkv * HALVES) * box_bytes);
                         for (int kv = 0; kv < nkv; ++kv)
 #pragma unroll
                             for (int h = 0; h < HALVES; ++h)
-                                tma_load_3d(st + (kv * HALVES + h) * half_stride + b * a.box_stride, &tmap, &full[s],
-                                            h * 64, row + kv * P, hg * Hc);
+                                tma_load_3d(st + (kv * HALVES + h) * half_stride, &tmap, &full[s], h * 64,
+                                            row + kv * P, hg * Hc);
                     }
+                    if (!ok) break;
+                }
+            } else {
+                // several boxes per chunk (pages below 16 slots): once the slot frees, all the
+                // chunk's page ids (up to 16 at page size 1) are loaded together, then its boxes
+                // are issued (not one dependent load per box)
+                for (int ti = t_begin; ti < t_end; ++ti) {
+                    const DecodeTile t = a.tiles[ti];
+                    const ChunkRange cr = chunk_range(t, P);
+                    bool ok = true;
+                    for (int k = cr.k0; k < cr.nk; ++k, ++it) {
+                        const int s = it % a.stages;
+                        const uint32_t use = it / a.stages;
+                        if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, err, kErrWaitEmpty)) {
+                            ok = false;
+                            break;
+                        }
+                        const int pos0 = cr.base + k * kDecodeKeysPerStage;
+                        const int nbox = min(nb, (cr.end - pos0 + kpb - 1) / kpb);
+                        int page[kDecodeKeysPerStage];
+#pragma unroll
+                        for (int b = 0; b < kDecodeKeysPerStage; ++b)
+                            if (b < nbox) page[b] = a.pages[t.kv_base + ((pos0 + b * kpb) >> a.page_shift)];
+                        uint8_t *st = smem + (size_t)s * a.stage_bytes;
+                        mbar_arrive_expect_tx(&full[s], (uint32_t)(nbox * nkv * HALVES) * box_bytes);
+#pragma unroll
+                        for (int b = 0; b < kDecodeKeysPerStage; ++b)
+                            if (b < nbox) {
+                                const int row = page[b] * 2 * P + ((pos0 + b * kpb) & (P - 1));
+                                for (int kv = 0; kv < nkv; ++kv)
+#pragma unroll
+                                    for (int h = 0; h < HALVES; ++h)
+                                        tma_load_3d(st + (kv * HALVES + h) * half_stride + b * a.box_stride, &tmap,
+                                                    &full[s], h * 64, row + kv * P, hg * Hc);
+                            }
+                    }
+                    if (!ok) break;
                 }
             }
             // Drain: every stage issued must have been consumed before the CTA exits.
             const uint32_t issued = it;
-            for (uint32_t k = issued > (uint32_t)a.stages ? issued - a.stages : 0; k < issued; ++k) {
-                const int s = k % a.stages;
-                if (!mbar_wait(&empty[s], (k / a.stages) & 1, err, kErrWaitDrain)) break;
+            for (uint32_t d = issued > (uint32_t)a.stages ? issued - a.stages : 0; d < issued; ++d) {
+                const int s = d % a.stages;
+                if (!mbar_wait(&empty[s], (d / a.stages) & 1, err, kErrWaitDrain)) break;
             }
         }
         return;
@@ -556,15 +591,11 @@ cudaError_t launch_gather(const Shape &s, const void *kv_layer, const int32_t *p
                       static_cast<uint4 *>(k_out), static_cast<uint4 *>(v_out));
 }
 
-static uint32_t decode_stage_bytes(const Shape &s) {
-    const uint32_t boxes = kDecodeKeysPerStage / s.dec_keys_per_box();
-    const uint32_t kv = s.dec_kv_in_box() ? 1u : 2u;
-    return kv * (uint32_t)(s.head_dim / 64) * boxes * (uint32_t)s.dec_box_stride();
-}
+static uint32_t decode_stage_bytes(const Shape &s) { return s.dec_stage_bytes(); }
 
 int decode_stages(const Shape &s) {
     const uint32_t sb = decode_stage_bytes(s);
-    int st = (int)((200u * 1024u) / sb);
+    int st = (int)(kDecodeRingBytes / (uint32_t)s.dec_ctas_per_sm() / sb);
     return st < 2 ? 0 : (st > dev::kDecodeMaxStages ? dev::kDecodeMaxStages : st);
 }
 

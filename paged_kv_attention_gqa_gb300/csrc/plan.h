@@ -23,6 +23,8 @@ constexpr int kPrefillRowsPerTile = 128;
 constexpr int kPrefillKeysPerStage = 64;
 // Keys per decode stage (one ring slot): two 8-key n-tiles of the QK^T MMA.
 constexpr int kDecodeKeysPerStage = 16;
+// Shared memory per SM given to decode rings (split among the SM's decode CTAs).
+constexpr uint32_t kDecodeRingBytes = 200u * 1024u;
 // A cut decode row with at most this many pieces is merged inside the decode kernel by
 // the CTA that finishes its last piece; longer ones by the separate merge kernel, whose
 // CTAs spread one row's heads over many SMs.
@@ -121,6 +123,18 @@ struct Shape {
         return 1;
     }
     int dec_head_groups() const { return num_kv_heads / dec_heads(); }
+    // Decode CTAs per SM: with fewer than 8 kv heads a CTA has few consumer warps, so
+    // several CTAs share an SM (and its 200 KB ring budget), up to 8 consumer warps and
+    // the warps the registers hold (16 at head_dim 64, 12 at 128, 8 at 256).
+    int dec_ctas_per_sm() const {
+        const int h = dec_heads();
+        const int warp_cap = head_dim <= 64 ? 16 : (head_dim <= 128 ? 12 : 8);
+        const int by_warps = warp_cap / (h + 1), by_heads = 8 / h;
+        const int by_smem = (int)(kDecodeRingBytes / (2u * dec_stage_bytes()));  // two stages each
+        int k = by_warps < by_heads ? by_warps : by_heads;
+        k = k < by_smem ? k : by_smem;
+        return k < 1 ? 1 : k;
+    }
     // Decode TMA boxes (64 columns x rows x dec_heads() heads, heads outermost).  From page
     // size 8 up a box holds min(P, 16) slots of K, and another the same slots of V; below
     // 8 one box holds a whole page, its P K rows followed by its P V rows (adjacent in the
@@ -130,6 +144,11 @@ struct Shape {
     int dec_box_rows() const { return dec_kv_in_box() ? 2 * page_size : dec_keys_per_box(); }
     // Bytes between boxes in shared memory: each box starts on a 1024-byte swizzle atom.
     int dec_box_stride() const { return (dec_box_rows() * dec_heads() * 128 + 1023) / 1024 * 1024; }
+    // One ring stage: the K and V boxes of a 16-key chunk, 64-column halves.
+    uint32_t dec_stage_bytes() const {
+        const uint32_t boxes = kDecodeKeysPerStage / dec_keys_per_box();
+        return (dec_kv_in_box() ? 1u : 2u) * (uint32_t)(head_dim / 64) * boxes * (uint32_t)dec_box_stride();
+    }
     // Prefill: rows of one paged TMA box (one head); pages smaller than 8 slots are
     // gathered with 16-byte cp.async copies instead (a box would not fill a swizzle atom).
     bool pf_gather() const { return page_size < 8; }

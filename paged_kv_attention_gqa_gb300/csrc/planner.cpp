@@ -205,9 +205,10 @@ int mixed_layout(const int32_t *qo, const int32_t *kvp, const int32_t *kvi, cons
 }
 
 int decode_cta_limit(const Shape &s) {
-    // One persistent decode CTA per SM: each holds a multi-stage ring of 16-key chunks of
-    // its kv heads; with several head groups the SMs are shared among them.
-    return std::max(1, s.sm_count / s.dec_head_groups());
+    // Persistent decode CTAs, Shape::dec_ctas_per_sm() per SM: each holds a multi-stage
+    // ring of 16-key chunks of its kv heads; with several head groups the SMs are shared
+    // among them.
+    return std::max(1, s.sm_count * s.dec_ctas_per_sm() / s.dec_head_groups());
 }
 
 // Keys each decode CTA is given at least (fewer per CTA would only multiply partials
