@@ -14,8 +14,8 @@
 //    V), so a CTA streams 16-key chunks of its heads: one producer thread issues TMA
 //    boxes (64-column halves, 128-byte swizzle) into a ring of stages, completion on an
 //    mbarrier; consumers release a stage through a second mbarrier.  A chunk is one box
-//    of K and one of V (page size >= 16), two of each (8), or 16 / P boxes each holding
-//    a whole page's K and V rows (P < 8).
+//    of K and one of V (page size >= 16) or two of each (8); pages below 8 slots are
+//    copied by the whole producer warp with 16-byte cp.async into the same layout.
 //  * One consumer warp per kv head.  The g query heads of the group are the M dimension of
 //    a 16x8x16 bf16 tensor-core MMA (padded to 16 rows); keys are N for QK^T and K for PV.
 //    Online softmax in the exp2 domain with quad shuffles.
@@ -58,7 +58,8 @@ struct DecodeArgs {
     int page_shift;    // log2 page_size
     int box_rows;      // rows per head of one TMA box
     int kpb_shift;     // log2 of the keys one box holds per head
-    int kv_in_box;     // 1: a box holds a page's K rows then its V rows
+    int gather;        // 1: pages below 8 slots, copied by the producer warps (cp.async)
+    int producers;     // producer warps (warps heads .. heads + producers - 1)
     int box_stride;    // bytes between boxes in a stage
     int stages;
     uint32_t stage_bytes;
@@ -122,7 +123,7 @@ __device__ __forceinline__ ChunkRange chunk_range(const DecodeTile &t, int P) {
 }
 
 // Byte offset, inside one 64-column half of a stage, of key `tok` (0..15) of local head
-// `hk`, and its 128-byte swizzle phase.  `vrow` = P when V rows follow K rows in a box.
+// `hk`, and its 128-byte swizzle phase (`vrow`: a row offset inside the box, 0 here).
 struct RowAddr {
     uint32_t off;
     uint32_t phase;
@@ -133,8 +134,10 @@ __device__ __forceinline__ RowAddr key_row(const DecodeArgs &a, int hk, int tok,
     return RowAddr{(uint32_t)(b * a.box_stride + row * 128), (uint32_t)(row & 7)};
 }
 
-template <int D, int G>
-__global__ void __launch_bounds__((D > 128 ? 4 : 8) * 32 + 32, 1)
+// SMALL: pages below 16 slots (several TMA boxes per chunk at 8 slots, cp.async producer
+// warps below 8); otherwise one box of K and one of V per chunk.
+template <int D, int G, bool SMALL>
+__global__ void __launch_bounds__((D > 128 ? 4 + (SMALL ? 2 : 1) : 8 + (SMALL ? 4 : 1)) * 32, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeArgs a) {
     constexpr int KS = D / 16;  // k-steps of QK^T
     constexpr int NT = D / 8;   // 8-wide output column tiles
@@ -160,11 +163,11 @@ __global__ void __launch_bounds__((D > 128 ? 4 : 8) * 32 + 32, 1)
     const int kpb = 1 << a.kpb_shift;
     const int nb = kDecodeKeysPerStage / kpb;
     const uint32_t half_stride = (uint32_t)nb * a.box_stride;
-    const uint32_t v_region = a.kv_in_box ? 0u : HALVES * half_stride;
+    const uint32_t v_region = HALVES * half_stride;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < a.stages; ++s) {
-            mbar_init(&full[s], 1);
+            mbar_init(&full[s], SMALL && a.gather ? 32 * a.producers : 1);  // gather: one per producer lane
             mbar_init(&empty[s], Hc);
         }
         fence_barrier_init();
@@ -174,13 +177,76 @@ __global__ void __launch_bounds__((D > 128 ? 4 : 8) * 32 + 32, 1)
     griddep_wait();  // inputs, the cache and the merge counters may come from the previous kernel
     griddep_launch();
 
-    if (warp == Hc) {
+    if (SMALL && a.gather && warp >= Hc) {
+        // ---------------- producers, pages below 8 slots: cp.async by `producers` warps ---
+        // (warp pw copies heads pw, pw + producers, ... of every chunk)
+        const int pw = warp - Hc;
+        // Lane = (key slot, 16-byte column chunk c), c fastest so that consecutive lanes copy
+        // consecutive bytes of one cache row; a warp instruction covers KPI keys.  The slot
+        // rows of the lane's keys are looked up once per chunk; keys past the piece's end
+        // read nothing and land as zeros.
+        constexpr int CH = D / 8;                       // 16-byte chunks per head row
+        constexpr int KPI = 32 / CH;                    // keys per warp instruction
+        constexpr int NI = kDecodeKeysPerStage / KPI;   // key iterations per chunk
+        const int c = lane % CH, kslot = lane / CH;
+        const size_t row_bytes = (size_t)a.num_kv_heads * D * 2;  // one slot row, all heads
+        const uint8_t *base = reinterpret_cast<const uint8_t *>(a.kv_layer) + (size_t)hg * Hc * D * 2 + c * 16;
+        uint32_t it = 0;
+        bool ok = true;
+        for (int ti = t_begin; ti < t_end && ok; ++ti) {
+            const DecodeTile t = a.tiles[ti];
+            const ChunkRange cr = chunk_range(t, P);
+            for (int k = cr.k0; k < cr.nk; ++k, ++it) {
+                const int s = it % a.stages;
+                const uint32_t use = it / a.stages;
+                const int pos0 = cr.base + k * kDecodeKeysPerStage;
+                int row[NI];
+#pragma unroll
+                for (int i = 0; i < NI; ++i) {
+                    const int pos = pos0 + kslot + KPI * i;
+                    row[i] = pos < cr.end ? a.pages[t.kv_base + (pos >> a.page_shift)] * 2 * P + (pos & (P - 1)) : -1;
+                }
+                bool w = true;
+                if (lane == 0 && use > 0) w = mbar_wait(&empty[s], (use - 1) & 1, err, kErrWaitEmpty);
+                if (!__shfl_sync(0xffffffffu, w ? 1 : 0, 0)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t st = smem_u32(smem + (size_t)s * a.stage_bytes) + (c >> 3) * half_stride;
+                for (int kv = 0; kv < 2; ++kv)
+                    for (int hh = pw; hh < Hc; hh += a.producers) {
+                        const uint8_t *src_h = base + (size_t)hh * D * 2 + (size_t)kv * P * row_bytes;
+                        const uint32_t dst_h = st + kv * HALVES * half_stride + hh * kDecodeKeysPerStage * 128;
+#pragma unroll
+                        for (int i = 0; i < NI; ++i) {
+                            const int key = kslot + KPI * i;
+                            const bool valid = row[i] >= 0;
+                            cp_async16(dst_h + key * 128 + (((c & 7) ^ (key & 7)) << 4),
+                                       valid ? src_h + (size_t)row[i] * row_bytes : base, valid ? 16u : 0u);
+                        }
+                    }
+                cp_async_mbar_arrive(&full[s]);
+            }
+        }
+        cp_async_wait_all();
+        // Drain: every stage issued must have been consumed before the CTA exits.
+        if (pw == 0 && lane == 0) {
+            const uint32_t issued = it;
+            for (uint32_t d = issued > (uint32_t)a.stages ? issued - a.stages : 0; d < issued; ++d) {
+                const int s = d % a.stages;
+                if (!mbar_wait(&empty[s], (d / a.stages) & 1, err, kErrWaitDrain)) break;
+            }
+        }
+        return;
+    }
+    if (warp >= Hc) {
+        if (warp > Hc) return;
         // ---------------- producer ----------------
         if (lane == 0) {
-            const int nkv = a.kv_in_box ? 1 : 2;
+            const int nkv = 2;
             const uint32_t box_bytes = (uint32_t)a.box_rows * Hc * 128;
             uint32_t it = 0;
-            if (nb == 1) {
+            if (!SMALL) {
                 // one box (of K and of V) per chunk: its page id is loaded after the slot frees
                 for (int ti = t_begin; ti < t_end; ++ti) {
                     const DecodeTile t = a.tiles[ti];
@@ -264,7 +330,7 @@ __global__ void __launch_bounds__((D > 128 ? 4 : 8) * 32 + 32, 1)
     const int k_chk = (lane >> 3) & 1;
     const int v_tok = (lane & 7) + (((lane >> 3) & 1) << 3);
     const int v_chk = lane >> 4;
-    const int vrow = a.kv_in_box ? P : 0;
+    const int vrow = 0;
     const RowAddr ka = key_row(a, hk, k_tok, 0);
     RowAddr va = key_row(a, hk, v_tok, vrow);
     va.off += v_region;
@@ -611,17 +677,18 @@ cudaError_t set_smem_limit(const void *fn, size_t smem, cudaStream_t st) {
     return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
 }
 
-template <int D, int G>
+template <int D, int G, bool SMALL>
 static cudaError_t launch_decode_t(const CUtensorMap &tm, const dev::DecodeArgs &a, dim3 grid, int warps, size_t smem,
                                    cudaStream_t st) {
-    auto fn = dev::decode_kernel<D, G>;
+    auto fn = dev::decode_kernel<D, G, SMALL>;
     cudaError_t e = set_smem_limit((const void *)fn, smem, st);
     if (e != cudaSuccess) return e;
     return launch_pdl(fn, grid, dim3(warps * 32), smem, st, tm, a);
 }
 
-cudaError_t launch_decode(const Shape &s, const Plan &p, const CUtensorMap &tm, void *ws, const void *q, void *out,
-                          float *lse, cudaStream_t st, const void *k_new, const void *v_new, void *kv_layer) {
+cudaError_t launch_decode(const Shape &s, const Plan &p, const CUtensorMap &tm, void *ws, const void *q,
+                          void *kv_layer, void *out, float *lse, cudaStream_t st, const void *k_new,
+                          const void *v_new) {
     const StaticCounts sc = static_counts(s, p.mode);
     const int grid = s.graph_static ? sc.dec_ctas : p.dec_ctas;
     if (grid == 0) return cudaSuccess;
@@ -648,17 +715,21 @@ cudaError_t launch_decode(const Shape &s, const Plan &p, const CUtensorMap &tm, 
     a.page_shift = s.page_shift();
     a.box_rows = s.dec_box_rows();
     a.kpb_shift = __builtin_ctz((unsigned)s.dec_keys_per_box());
-    a.kv_in_box = s.dec_kv_in_box() ? 1 : 0;
+    a.gather = s.dec_gather() ? 1 : 0;
+    a.producers = s.dec_producer_warps();
     a.box_stride = s.dec_box_stride();
     a.stages = decode_stages(s);
     a.stage_bytes = decode_stage_bytes(s);
     if (a.stages == 0) return cudaErrorInvalidValue;
-    const int warps = a.heads + 1;
+    const int warps = a.heads + a.producers;
     const size_t smem = decode_smem_bytes(s);
     cudaError_t e = cudaErrorInvalidValue;
     const int g = s.group();
-#define PKV_DEC(DD, GG) \
-    if (s.head_dim == DD && g == GG) e = launch_decode_t<DD, GG>(tm, a, dim3(grid, s.dec_head_groups()), warps, smem, st);
+#define PKV_DEC(DD, GG)                                                                                  \
+    if (s.head_dim == DD && g == GG)                                                                      \
+        e = s.page_size < 16                                                                               \
+                ? launch_decode_t<DD, GG, true>(tm, a, dim3(grid, s.dec_head_groups()), warps, smem, st)          \
+                : launch_decode_t<DD, GG, false>(tm, a, dim3(grid, s.dec_head_groups()), warps, smem, st);
     PKV_FOR_EACH_HEAD_DIM_AND_GROUP(PKV_DEC)
 #undef PKV_DEC
     if (e != cudaSuccess) return e;

@@ -41,11 +41,12 @@ cudaError_t launch_append(const Shape &s, const Plan &p, void *ws, const void *k
                           cudaStream_t st);
 // Decode pass (and the split-KV merge) of a DECODE or MIXED plan; `tm` boxes
 // (64 columns, Shape::dec_box_rows() rows, Shape::dec_heads() heads) of the layer slice.
-// With k_new / v_new / kv_layer given (a DECODE plan), the kernel also appends the plan's
-// new tokens (the pieces holding each row's last position store them).
-cudaError_t launch_decode(const Shape &s, const Plan &p, const CUtensorMap &tm, void *ws, const void *q, void *out,
-                          float *lse, cudaStream_t st, const void *k_new = nullptr, const void *v_new = nullptr,
-                          void *kv_layer = nullptr);
+// `kv_layer` is the slice `tm` maps (read directly for pages below 8 slots).  With k_new /
+// v_new given (a DECODE plan), the kernel also appends the plan's new tokens (the pieces
+// holding each row's last position store them into kv_layer).
+cudaError_t launch_decode(const Shape &s, const Plan &p, const CUtensorMap &tm, void *ws, const void *q,
+                          void *kv_layer, void *out, float *lse, cudaStream_t st, const void *k_new = nullptr,
+                          const void *v_new = nullptr);
 // Prefill pass of a PREFILL, MIXED or DENSE plan; `tm_kv` boxes Shape::pf_box_rows() rows
 // of one kv head of the layer slice (paged; V rows follow K rows by page_size) or 16 rows
 // of contiguous K (dense, with `tm_v` over contiguous V); `tm_q` boxes (64 columns, g

@@ -303,8 +303,8 @@ extern "C" pkv_status pkv_run_decode(pkv_handle_t h, const void *q, const void *
     if (h->plan.batch == 0) return PKV_OK;
     if ((st = check_io(h, q, kv_layer, out)) != PKV_OK) return st;
     if ((st = dec_map(h, kv_layer)) != PKV_OK) return st;
-    cudaError_t e = pkv::launch_decode(h->shape, h->plan, h->tm_dec, workspace, q, out, lse,
-                                       static_cast<cudaStream_t>(stream));
+    cudaError_t e = pkv::launch_decode(h->shape, h->plan, h->tm_dec, workspace, q, const_cast<void *>(kv_layer), out,
+                                       lse, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PKV_OK : cuda_fail(h, e, "decode launch");
 }
 
@@ -319,8 +319,8 @@ extern "C" pkv_status pkv_run_decode_append(pkv_handle_t h, const void *q, const
     if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(kv_layer)) % 16)
         return fail(h, PKV_ERR_INVALID, "k, v and kv_layer must be 16-byte aligned");
     if ((st = dec_map(h, kv_layer)) != PKV_OK) return st;
-    cudaError_t e = pkv::launch_decode(h->shape, h->plan, h->tm_dec, workspace, q, out, lse,
-                                       static_cast<cudaStream_t>(stream), k, v, kv_layer);
+    cudaError_t e = pkv::launch_decode(h->shape, h->plan, h->tm_dec, workspace, q, kv_layer, out, lse,
+                                       static_cast<cudaStream_t>(stream), k, v);
     return e == cudaSuccess ? PKV_OK : cuda_fail(h, e, "decode + append launch");
 }
 
@@ -360,7 +360,7 @@ extern "C" pkv_status pkv_run_mixed(pkv_handle_t h, const void *q, const void *k
     e = cudaEventRecord(h->ev_fork, s);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(h->side, h->ev_fork, 0);
     if (e != cudaSuccess) return cuda_fail(h, e, "mixed fork");
-    e = pkv::launch_decode(h->shape, h->plan, h->tm_dec, workspace, q, out, lse, s);
+    e = pkv::launch_decode(h->shape, h->plan, h->tm_dec, workspace, q, const_cast<void *>(kv_layer), out, lse, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "mixed decode-pass launch");
     e = pkv::launch_prefill(h->shape, h->plan, h->tm_pf, h->tm_pf, h->tm_q, kv_layer, workspace, out, lse, h->side);
     if (e != cudaSuccess) return cuda_fail(h, e, "mixed prefill-pass launch");
@@ -489,7 +489,7 @@ extern "C" pkv_status pkv_run_decode_static(pkv_handle_t h, const void *q, const
     // The plan image (its error word zeroed) overwrites the previous call's contents.
     e = cudaMemcpyAsync(scratch, plan.image.data(), plan.image.size(), cudaMemcpyHostToDevice, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "static plan H2D");
-    e = pkv::launch_decode(h->shape, plan, h->tm_dec, scratch, q, out, lse, s);
+    e = pkv::launch_decode(h->shape, plan, h->tm_dec, scratch, q, const_cast<void *>(kv_layer), out, lse, s);
     return e == cudaSuccess ? PKV_OK : cuda_fail(h, e, "static decode launch");
 }
 

@@ -129,25 +129,33 @@ struct Shape {
     int dec_ctas_per_sm() const {
         const int h = dec_heads();
         const int warp_cap = head_dim <= 64 ? 16 : (head_dim <= 128 ? 12 : 8);
-        const int by_warps = warp_cap / (h + 1), by_heads = 8 / h;
+        const int by_warps = warp_cap / (h + dec_producer_warps()), by_heads = 8 / h;
         const int by_smem = (int)(kDecodeRingBytes / (2u * dec_stage_bytes()));  // two stages each
         int k = by_warps < by_heads ? by_warps : by_heads;
         k = k < by_smem ? k : by_smem;
         return k < 1 ? 1 : k;
     }
-    // Decode TMA boxes (64 columns x rows x dec_heads() heads, heads outermost).  From page
-    // size 8 up a box holds min(P, 16) slots of K, and another the same slots of V; below
-    // 8 one box holds a whole page, its P K rows followed by its P V rows (adjacent in the
-    // cache), so that a box is never smaller than 8 rows for 8 heads.
-    bool dec_kv_in_box() const { return page_size < 8; }
-    int dec_keys_per_box() const { return page_size < 16 ? page_size : 16; }
-    int dec_box_rows() const { return dec_kv_in_box() ? 2 * page_size : dec_keys_per_box(); }
-    // Bytes between boxes in shared memory: each box starts on a 1024-byte swizzle atom.
-    int dec_box_stride() const { return (dec_box_rows() * dec_heads() * 128 + 1023) / 1024 * 1024; }
+    // Decode TMA boxes (64 columns x rows x dec_heads() heads, heads outermost): 16 slots of
+    // K and the same 16 of V per box pair from page size 16 up, 8 at page size 8.  Pages
+    // below 8 slots are gathered by the producer warp with 16-byte cp.async copies into the
+    // page-16 layout instead: a box of one such page would be smaller than a swizzle atom,
+    // and keys in separate atoms would put an ldmatrix's 8 rows on the same banks.
+    bool dec_gather() const { return page_size < 8; }
+    // Producer warps of a decode CTA: one thread issues TMA; the cp.async gather takes one
+    // warp per two kv heads of the CTA (1 to 4), each copying its share of the heads.
+    int dec_producer_warps() const {
+        if (!dec_gather()) return 1;
+        const int w = dec_heads() / 2;
+        return w < 1 ? 1 : (w > 4 ? 4 : w);
+    }
+    int dec_keys_per_box() const { return page_size == 8 ? 8 : 16; }
+    int dec_box_rows() const { return dec_keys_per_box(); }
+    // Bytes between boxes in shared memory (a multiple of the 1024-byte swizzle atom).
+    int dec_box_stride() const { return dec_box_rows() * dec_heads() * 128; }
     // One ring stage: the K and V boxes of a 16-key chunk, 64-column halves.
     uint32_t dec_stage_bytes() const {
         const uint32_t boxes = kDecodeKeysPerStage / dec_keys_per_box();
-        return (dec_kv_in_box() ? 1u : 2u) * (uint32_t)(head_dim / 64) * boxes * (uint32_t)dec_box_stride();
+        return 2u * (uint32_t)(head_dim / 64) * boxes * (uint32_t)dec_box_stride();
     }
     // Prefill: rows of one paged TMA box (one head); pages smaller than 8 slots are
     // gathered with 16-byte cp.async copies instead (a box would not fill a swizzle atom).
