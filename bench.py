@@ -601,23 +601,36 @@ def shape_lines(B, dev, peaks, seed, flush):
     return out
 
 
-def cpu_baseline(pb, seed, window, reps=1):
-    """The oracle as it stands on the host cores, on one layer of the same workload."""
+def cpu_baseline(pb, seed, window, seconds=10.0, one_core_seconds=5.0):
+    """The oracle as it stands on the host cores, on one layer of the same workload: passes
+    over that layer repeated for about `seconds` on all host threads, and for about
+    `one_core_seconds` on one thread."""
     import oracle
     x = wl.make_inputs(pb, device="cuda" if torch.cuda.is_available() else "cpu", seed=seed, unused="randn",
                        layers=1)
     qb, kvb = wl.bf16_bits(x["q"]), wl.bf16_bits(x["kv_cache"][0])
     del x
+
+    def timed(threads, budget):
+        passes, s0 = 0, time.perf_counter()
+        while True:
+            oracle.attention(qb, kvb, pb.qo_indptr, pb.kv_indptr, pb.kv_indices, pb.last_page_len,
+                             num_qo_heads=pb.num_qo_heads, num_kv_heads=pb.num_kv_heads, head_dim=pb.head_dim,
+                             page_size=pb.page_size, window_left=window, threads=threads)
+            passes += 1
+            el = time.perf_counter() - s0
+            if el >= budget or passes >= 1000:
+                return passes, el
+
+    layer_bytes = decode_kv_bytes(pb, window)
     threads = os.cpu_count() or 1
-    s0 = time.perf_counter()
-    for _ in range(reps):
-        oracle.attention(qb, kvb, pb.qo_indptr, pb.kv_indptr, pb.kv_indices, pb.last_page_len,
-                         num_qo_heads=pb.num_qo_heads, num_kv_heads=pb.num_kv_heads, head_dim=pb.head_dim,
-                         page_size=pb.page_size, window_left=window, threads=threads)
-    sec = (time.perf_counter() - s0) / reps
-    return {"value": round(decode_kv_bytes(pb, window) / sec / 1e9, 3), "unit": "GB/s", "cores": threads,
-            "kind": "oracle", "sample": f"layer 0 of {pb.num_layers} ({pb.batch} rows), {reps} pass(es), "
-                                        f"{sec:.2f} s; rows split over {threads} threads"}
+    n, el = timed(threads, seconds)
+    n1, el1 = timed(1, one_core_seconds)
+    return {"value": round(layer_bytes * n / el / 1e9, 3), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"layer 0 of {pb.num_layers} ({pb.batch} rows), {n} passes in {el:.1f} s, rows split over "
+                      f"{threads} threads",
+            "one_core": {"value": round(layer_bytes * n1 / el1 / 1e9, 3), "unit": "GB/s", "cores": 1,
+                         "sample": f"the same layer, {n1} passes in {el1:.1f} s on one thread"}}
 
 
 # ----------------------------------------------------------------------------- reference arm
