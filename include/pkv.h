@@ -241,6 +241,15 @@ pkv_status pkv_gather_kv(pkv_handle_t h, const void *kv_layer, const int32_t *pa
 pkv_status pkv_check_device_error(pkv_handle_t h, void *workspace, pkv_stream_t stream, int *code);
 
 /*
+ * Self-test of that error path (no counterpart on the pages): one device thread waits,
+ * for `polls` polls (1..2^20), on a barrier nothing arrives on, gives up, records error
+ * code 4 in the workspace's error word and returns -- no trap, no hang.  A following
+ * pkv_check_device_error reports PKV_ERR_DEVICE with code 4 and clears the word; the
+ * handle, the workspace and the CUDA context stay usable.  Needs a plan on `workspace`.
+ */
+pkv_status pkv_selftest_wait_timeout(pkv_handle_t h, void *workspace, int polls, pkv_stream_t stream);
+
+/*
  * Decode that needs no workspace: plan + pkv_run_decode in one call, with the plan and
  * the split-KV partials kept in a 16 MiB scratch array compiled into the library
  * (one per GPU that loads it, held until the process exits).  The pages have no

@@ -24,7 +24,7 @@ STATUS_NAMES = ["OK", "INVALID", "UNSUPPORTED", "WORKSPACE", "TOO_MANY_PREFILL_R
 EXPORTS = ["pkv_create", "pkv_destroy", "pkv_last_error", "pkv_workspace_size", "pkv_plan", "pkv_kv_append",
            "pkv_run_decode", "pkv_run_prefill", "pkv_run_mixed", "pkv_check_device_error", "pkv_append_slots",
            "pkv_mixed_layout", "pkv_decode_split", "pkv_run_decode_static", "pkv_context_only_views",
-           "pkv_plan_dense", "pkv_run_dense", "pkv_gather_kv", "pkv_run_decode_append"]
+           "pkv_plan_dense", "pkv_run_dense", "pkv_gather_kv", "pkv_run_decode_append", "pkv_selftest_wait_timeout"]
 
 
 class PkvError(RuntimeError):
@@ -61,6 +61,7 @@ def load(path: str = LIB_PATH):
         "pkv_kv_append": ([vp, vp, vp, vp, vp, vp], i),
         "pkv_run_decode": ([vp, vp, vp, vp, vp, vp, vp], i),
         "pkv_run_decode_append": ([vp, vp, vp, vp, vp, vp, vp, vp, vp], i),
+        "pkv_selftest_wait_timeout": ([vp, vp, i, vp], i),
         "pkv_run_prefill": ([vp, vp, vp, vp, vp, vp, vp], i),
         "pkv_run_mixed": ([vp, vp, vp, vp, vp, vp, vp], i),
         "pkv_check_device_error": ([vp, vp, vp, ctypes.POINTER(i)], i),
@@ -186,6 +187,10 @@ class Handle:
         """pages: a device int32 tensor of page ids."""
         self._check(self.lib.pkv_gather_kv(self.h, _dptr(kv_layer), _dptr(pages), int(num_tokens), _dptr(k_out),
                                            _dptr(v_out), _stream(stream)))
+
+    def selftest_wait_timeout(self, workspace, polls=1000, stream=None):
+        """Make one device wait give up (see pkv.h); check_device_error then reports code 4."""
+        self._check(self.lib.pkv_selftest_wait_timeout(self.h, _dptr(workspace), int(polls), _stream(stream)))
 
     def check_device_error(self, workspace, stream=None) -> int:
         code = ctypes.c_int()

@@ -642,7 +642,25 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint4 *cache, const i
     }
 }
 
+// Self-test of the device error path: one thread waits, with `polls` polls, on an mbarrier
+// nothing ever arrives on; the wait gives up, records kErrWaitSelfTest in the plan's error
+// word and the kernel returns (no fault, no hang, the context stays usable).
+__global__ void __launch_bounds__(32) selftest_wait_kernel(PlanHeader *hdr, uint32_t polls) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_barrier_init();
+        mbar_wait(&bar, 0, &hdr->err, kErrWaitSelfTest, polls);
+    }
+}
+
 }  // namespace dev
+
+cudaError_t launch_selftest_wait(const Plan &p, void *ws, uint32_t polls, cudaStream_t st) {
+    dev::selftest_wait_kernel<<<1, 32, 0, st>>>(
+        reinterpret_cast<PlanHeader *>(static_cast<uint8_t *>(ws) + p.lay.err), polls);
+    return cudaGetLastError();
+}
 
 // ------------------------------------------------------------------------------------
 // launchers

@@ -60,6 +60,9 @@ cudaError_t launch_prefill(const Shape &s, const Plan &p, const CUtensorMap &tm_
 cudaError_t launch_gather(const Shape &s, const void *kv_layer, const int32_t *pages, int num_tokens, void *k_out,
                           void *v_out, cudaStream_t st);
 
+// Self-test of the device error path (pkv_selftest_wait_timeout).
+cudaError_t launch_selftest_wait(const Plan &p, void *ws, uint32_t polls, cudaStream_t st);
+
 // File-scope device scratch used by pkv_run_decode_static (see decode.cu).
 size_t static_scratch_bytes();
 cudaError_t static_scratch(void **ptr);

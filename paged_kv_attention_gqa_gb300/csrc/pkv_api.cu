@@ -389,6 +389,14 @@ extern "C" pkv_status pkv_check_device_error(pkv_handle_t h, void *workspace, pk
     return PKV_OK;
 }
 
+extern "C" pkv_status pkv_selftest_wait_timeout(pkv_handle_t h, void *workspace, int polls, pkv_stream_t stream) {
+    if (!h || !workspace) return fail(h, PKV_ERR_INVALID, "null argument");
+    if (polls < 1 || polls > (1 << 20)) return fail(h, PKV_ERR_INVALID, "polls must be in [1, 2^20]");
+    if (h->planned_ws != workspace) return fail(h, PKV_ERR_NOT_PLANNED, "no plan on this workspace");
+    cudaError_t e = pkv::launch_selftest_wait(h->plan, workspace, (uint32_t)polls, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : cuda_fail(h, e, "self-test launch");
+}
+
 // ---------------- host-only queries ----------------
 
 extern "C" pkv_status pkv_append_slots(int page_size, const int32_t *qo, const int32_t *kvp, const int32_t *kvi,

@@ -11,7 +11,7 @@ namespace dev {
 // try_wait), records an error word and lets the kernel run to its end.
 constexpr uint32_t kWaitLimit = 1u << 22;
 
-enum DeviceError : int { kErrWaitFull = 1, kErrWaitEmpty = 2, kErrWaitDrain = 3 };
+enum DeviceError : int { kErrWaitFull = 1, kErrWaitEmpty = 2, kErrWaitDrain = 3, kErrWaitSelfTest = 4 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -48,9 +48,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Wait for the phase with `parity` to complete.  Returns false (after recording `code`
-// in *err) if it does not complete within kWaitLimit polls.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *err, int code) {
-    for (uint32_t i = 0; i < kWaitLimit; ++i)
+// in *err) if it does not complete within `limit` polls.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *err, int code,
+                                          uint32_t limit = kWaitLimit) {
+    for (uint32_t i = 0; i < limit; ++i)
         if (mbar_try_wait(bar, parity)) return true;
     if (err) atomicCAS(err, 0, code);
     return false;
