@@ -277,3 +277,69 @@ def test_graph_mode_shapes(P, D, Hq, Hkv):
         assert np.array_equal(wl.bf16_bits(kv), after)
         ref_o, ref_l = G.oracle_attn(pb, wl.bf16_bits(x["q"]), after)
         G.compare(out, lse, ref_o, ref_l, what=f"graph P{P} D{D} plan {i}")
+
+
+def test_mixed_head_dim_256():
+    n = [1, 40, 1, 3, 1, 100]
+    c = [20, 10, 700, 0, 16, 33]
+    pb = wl.custom(260, np.add(n, c), n, num_qo_heads=16, num_kv_heads=8, head_dim=256, page_size=16,
+                   reserve_sink=True)
+    pb.max_prefill_rows = int((np.asarray(n) >= 2).sum()) + 1
+    _check_step(pb, "mixed", seed=12)
+
+
+@pytest.mark.parametrize("P", [2, 32])
+def test_graph_mode_prefill_page_sizes(P):
+    """Prefill (cp.async gather below 8 slots, TMA above) captured once at the maxima,
+    replayed for a second plan of another shape of rows."""
+    from paged_kv_attention_gqa_gb300 import binding as B
+    steps = [([5, 40, 130], [0, 300, 17]), ([64, 1], [900, 3])]
+    pbs = [wl.custom(270 + i, np.add(n, c), n, num_qo_heads=16, num_kv_heads=4, head_dim=128, page_size=P,
+                     pool_pages=2048 // P + 64) for i, (n, c) in enumerate(steps)]
+    T = max(pb.num_tokens for pb in pbs)
+    h = B.Handle(num_qo_heads=16, num_kv_heads=4, head_dim=128, page_size=P, max_batch=3, max_total_tokens=T,
+                 max_num_pages=max(len(pb.kv_indices) for pb in pbs) + 8, num_cache_pages=pbs[0].max_pages,
+                 max_prefill_rows=3, graph_static=1)
+    ws = torch.empty(h.workspace_size(B.MODE_PREFILL), dtype=torch.uint8, device="cuda")
+    q = torch.zeros(T, 16, 128, dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros(T, 4, 128, dtype=torch.bfloat16, device="cuda")
+    v = torch.zeros_like(k)
+    out = torch.zeros_like(q)
+    lse = torch.zeros(T, 16, dtype=torch.float32, device="cuda")
+    kv = torch.zeros(pbs[0].max_pages, 2, P, 4, 128, dtype=torch.bfloat16, device="cuda")
+
+    def load(pb, seed):
+        x = wl.make_inputs(pb, device="cuda", seed=seed, unused="nan", layers=1)
+        n = pb.num_tokens
+        q[:n].copy_(x["q"])
+        k[:n].copy_(x["k_new"])
+        v[:n].copy_(x["v_new"])
+        kv.copy_(x["kv_cache"][0])
+        return x
+
+    def plan(pb):
+        h.plan(B.MODE_PREFILL, pb.qo_indptr, pb.kv_indptr, pb.kv_indices, pb.last_page_len, workspace=ws)
+
+    load(pbs[0], 20)
+    plan(pbs[0])
+    h.kv_append(k, v, kv, workspace=ws)
+    h.run_prefill(q, kv, out, lse, workspace=ws)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        h.kv_append(k, v, kv, workspace=ws)
+        h.run_prefill(q, kv, out, lse, workspace=ws)
+    torch.cuda.synchronize()
+    for i, pb in enumerate(pbs[::-1]):
+        x = load(pb, 21 + i)
+        before = wl.bf16_bits(kv)
+        out.fill_(float("nan"))
+        plan(pb)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert h.check_device_error(ws) == 0
+        after = G.oracle_append(pb, before, x)
+        assert np.array_equal(wl.bf16_bits(kv), after)
+        n = pb.num_tokens
+        ref_o, ref_l = G.oracle_attn(pb, wl.bf16_bits(x["q"]), after)
+        G.compare(out[:n], lse[:n], ref_o, ref_l, what=f"graph prefill P{P} plan {i}")
