@@ -98,20 +98,22 @@ __global__ void __launch_bounds__(GATHER ? kPfGatherThreads : kPfThreads, D > 12
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::BAR_OFF);
+    // Each MMA group commits to one barrier that every party waiting on it polls by
+    // parity: s_full[s] (S_j done: the softmax may read it, K slot s is free again) and
+    // pv_done[s] (PV_j done: V slot s is free, S buffer s may be overwritten, O holds
+    // P_0..P_j V).  A waiter is never two phases behind, because the next phase of either
+    // barrier needs data that the waiter itself has yet to provide.
     uint64_t *q_full = bars + 0;
     uint64_t *k_full = bars + 1;   // [2]
     uint64_t *v_full = bars + 3;   // [2]
-    uint64_t *k_empty = bars + 5;  // [2]
-    uint64_t *v_empty = bars + 7;  // [2]
-    uint64_t *s_full = bars + 9;   // [2]
-    uint64_t *p_full = bars + 11;  // [2]
-    uint64_t *o_done = bars + 13;
-    uint64_t *pv_done = bars + 14;  // [2]: PV_i, which reads P_i from S buffer i & 1, has completed
-    // o_final completes once, after the last PV.  The epilogue cannot wait on o_done by
-    // parity: when it gets there, two PVs may still be outstanding, and phase nt-1 has
-    // the same parity as the already completed phase nt-3.
-    uint64_t *o_final = bars + 16;
-    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 17);
+    uint64_t *s_full = bars + 5;   // [2]
+    uint64_t *p_full = bars + 7;   // [2]
+    uint64_t *pv_done = bars + 9;  // [2]
+    // o_final completes once, after the last PV.  The epilogue cannot wait on pv_done by
+    // parity: when it gets there, two PVs may still be outstanding, and phase (nt-1)/2 of
+    // one buffer's barrier has the same parity as an already completed earlier phase.
+    uint64_t *o_final = bars + 11;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 12);
 
     if ((int)blockIdx.x >= a.hdr->pf_tiles) return;  // an idle CTA of a launch at the maxima
     const PrefillTile t = a.tiles[blockIdx.x];
@@ -132,13 +134,10 @@ __global__ void __launch_bounds__(GATHER ? kPfGatherThreads : kPfThreads, D > 12
         for (int s = 0; s < 2; ++s) {
             mbar_init(&k_full[s], GATHER ? kPfGatherWarps : 1);  // gather: one per producer warp
             mbar_init(&v_full[s], GATHER ? kPfGatherWarps : 1);
-            mbar_init(&k_empty[s], 1);
-            mbar_init(&v_empty[s], 1);
             mbar_init(&s_full[s], 1);
             mbar_init(&p_full[s], 4);
             mbar_init(&pv_done[s], 1);
         }
-        mbar_init(o_done, 1);
         mbar_init(o_final, 1);
         fence_barrier_init();
     }
@@ -206,7 +205,7 @@ __global__ void __launch_bounds__(GATHER ? kPfGatherThreads : kPfThreads, D > 12
                 for (int j = 0; j < nt; ++j) {
                     const int s = j & 1;
                     const uint32_t use = j >> 1;
-                    if (use > 0 && !mbar_wait(&k_empty[s], (use - 1) & 1, err, kErrWaitEmpty)) break;
+                    if (use > 0 && !mbar_wait(&s_full[s], (use - 1) & 1, err, kErrWaitEmpty)) break;
                     uint8_t *kd = sm + L::K_OFF + s * L::KV_BYTES;
                     mbar_arrive_expect_tx(&k_full[s], L::KV_BYTES);
 #pragma unroll
@@ -218,7 +217,7 @@ __global__ void __launch_bounds__(GATHER ? kPfGatherThreads : kPfThreads, D > 12
                     // the next tile's page ids load while this tile's V slot drains: by the
                     // time the next K slot is free (it frees before this V slot) they are here
                     if (j + 1 < nt) tile_rows(j + 1, next);
-                    if (use > 0 && !mbar_wait(&v_empty[s], (use - 1) & 1, err, kErrWaitEmpty)) break;
+                    if (use > 0 && !mbar_wait(&pv_done[s], (use - 1) & 1, err, kErrWaitEmpty)) break;
                     uint8_t *vd = sm + L::V_OFF + s * L::KV_BYTES;
                     mbar_arrive_expect_tx(&v_full[s], L::KV_BYTES);
 #pragma unroll
@@ -265,8 +264,8 @@ __global__ void __launch_bounds__(GATHER ? kPfGatherThreads : kPfThreads, D > 12
                 }
                 bool ok = true;
                 if (lane == 0 && use > 0)
-                    ok = mbar_wait(&k_empty[s], (use - 1) & 1, err, kErrWaitEmpty) &&
-                         mbar_wait(&v_empty[s], (use - 1) & 1, err, kErrWaitEmpty);
+                    ok = mbar_wait(&s_full[s], (use - 1) & 1, err, kErrWaitEmpty) &&
+                         mbar_wait(&pv_done[s], (use - 1) & 1, err, kErrWaitEmpty);
                 if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
                 const uint32_t kd = smem_u32(sm + L::K_OFF + s * L::KV_BYTES) + (c >> 3) * (L::KV_BYTES / HALVES);
                 const uint32_t vd = smem_u32(sm + L::V_OFF + s * L::KV_BYTES) + (c >> 3) * (L::KV_BYTES / HALVES);
@@ -324,8 +323,6 @@ __global__ void __launch_bounds__(GATHER ? kPfGatherThreads : kPfThreads, D > 12
                     const uint64_t bd = smem_desc(sV + kk * 2048, L::KV_BYTES / HALVES, 1024, kSwizzle128B);
                     mma_ts(O_col, S_col[s] + kk * 8, bd, ID_O, (i > 0 || kk > 0) ? 1u : 0u);
                 }
-                mma_commit(o_done);
-                mma_commit(&v_empty[s]);
                 mma_commit(&pv_done[s]);
             }
             __syncwarp();
@@ -349,7 +346,6 @@ __global__ void __launch_bounds__(GATHER ? kPfGatherThreads : kPfThreads, D > 12
                     mma_ss(S_col[s], ad, bd, ID_S, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(&s_full[s]);
-                mma_commit(&k_empty[s]);
             }
             __syncwarp();
             if (j >= 1) issue_pv(j - 1);
@@ -439,7 +435,7 @@ __global__ void __launch_bounds__(GATHER ? kPfGatherThreads : kPfThreads, D > 12
             tmem_wait_st();
             if (warp_grow) {
                 // O holds P_0..P_{j-1} V: wait for the last of those MMAs, then scale O rows
-                if (!mbar_wait(o_done, (j - 1) & 1, err, kErrWaitFull)) {
+                if (!mbar_wait(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, err, kErrWaitFull)) {
                     ok = false;
                     break;
                 }
