@@ -439,7 +439,9 @@ def run_step_primary(args, rank, world):
         value, unit = world * fl / (ms * 1e-3) / 1e12, "TFLOP/s"
         achieved = fl / (kms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": None, "kernel": "prefill_tc_kernel",
+                "frac": round(achieved / peaks["bf16_tflops"], 4),
+                "traffic": kernel_traffic("prefill_kernel.cuh", "prefill_ragged16_tcgen05.md"),
+                "kernel": "prefill_tc_kernel",
                 "launch_ms": round(kms, 5), "peak_source": peaks["source"]}
         launches = 2
     else:
@@ -516,7 +518,10 @@ def secondary(B, dev, peaks, seed):
     res["prefill"] = {"workload": "16 rows, new U[128,2048], prefix U[0,4096], 32/8/128, causal",
                       "ms": round(ms, 4), "tflops": round(tf, 1), "peak_tflops": peaks["bf16_tflops"],
                       "frac": round(tf / peaks["bf16_tflops"], 4), "tokens_per_s": round(pb.num_tokens / (ms * 1e-3)),
-                      "append_ms": round(app_ms, 4)}
+                      "append_ms": round(app_ms, 4),
+                      # DRAM bytes of one launch from the committed ncu capture (None once the
+                      # kernel source differs from the captured one)
+                      "traffic": kernel_traffic("prefill_kernel.cuh", "prefill_ragged16_tcgen05.md")}
     del x, kv
     # mixed step
     pb = wl.config_mixed(seed=seed)
