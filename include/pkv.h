@@ -92,6 +92,11 @@ enum { PKV_NON_CAUSAL = 0, PKV_CAUSAL = 1, PKV_CONTEXT_ONLY = 2 };
  *                     the maxima (max_batch rows for decode, max_total_tokens otherwise).
  *                     Make one uncaptured call of each kind first (it sets kernel
  *                     attributes).  0 = launches sized to each plan.
+ *   enable_nvtx:      1 = every call on this handle opens an NVTX range named after it
+ *                     ("pkv_plan", "pkv_kv_append", "pkv_run_decode", ...) for its
+ *                     host-side duration, so a profiler's timeline shows the plan,
+ *                     append and run spans of a step (the wrappers' enable_nvtx).  With
+ *                     no profiler attached the ranges cost nothing.  0 = no ranges.
  */
 typedef struct {
     int num_qo_heads;
@@ -106,6 +111,7 @@ typedef struct {
     int sm_count;
     int sink_page;
     int graph_static;
+    int enable_nvtx;
 } pkv_config;
 
 /*

@@ -37,7 +37,8 @@ class PkvError(RuntimeError):
 class Config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "num_qo_heads", "num_kv_heads", "head_dim", "page_size", "max_batch", "max_total_tokens",
-        "max_num_pages", "num_cache_pages", "max_prefill_rows", "sm_count", "sink_page", "graph_static")]
+        "max_num_pages", "num_cache_pages", "max_prefill_rows", "sm_count", "sink_page", "graph_static",
+        "enable_nvtx")]
 
 
 _lib = None
@@ -110,10 +111,12 @@ class Handle:
     """One pkv handle: static shape and the last plan (see include/pkv.h)."""
 
     def __init__(self, *, num_qo_heads, num_kv_heads, head_dim, page_size, max_batch, max_total_tokens=0,
-                 max_num_pages, num_cache_pages, max_prefill_rows=0, sm_count=0, sink_page=-1, graph_static=0):
+                 max_num_pages, num_cache_pages, max_prefill_rows=0, sm_count=0, sink_page=-1, graph_static=0,
+                 enable_nvtx=False):
         self.lib = load()
         self.cfg = Config(num_qo_heads, num_kv_heads, head_dim, page_size, max_batch, max_total_tokens,
-                          max_num_pages, num_cache_pages, max_prefill_rows, sm_count, sink_page, int(graph_static))
+                          max_num_pages, num_cache_pages, max_prefill_rows, sm_count, sink_page, int(graph_static),
+                          int(enable_nvtx))
         h = ctypes.c_void_p()
         st = self.lib.pkv_create(ctypes.byref(self.cfg), ctypes.byref(h))
         if st != OK:

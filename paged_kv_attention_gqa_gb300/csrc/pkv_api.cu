@@ -2,6 +2,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <cmath>
 #include <cstdio>
@@ -35,6 +36,19 @@ struct pkv_handle_s {
     const void *tm_dec_ptr = nullptr, *tm_pf_ptr = nullptr, *tm_q_ptr = nullptr;
     int tm_q_rows = -1;
     CUtensorMap tm_dec{}, tm_pf{}, tm_q{};
+    bool nvtx = false;  // one NVTX range per call (pkv_config.enable_nvtx)
+};
+
+// The NVTX range of one call on a handle with enable_nvtx set: opened here, closed when
+// the call returns.
+struct NvtxCall {
+    bool on;
+    NvtxCall(const pkv_handle_s *h, const char *name) : on(h && h->nvtx) {
+        if (on) nvtxRangePushA(name);
+    }
+    ~NvtxCall() {
+        if (on) nvtxRangePop();
+    }
 };
 
 static thread_local std::string g_create_err;
@@ -73,6 +87,7 @@ extern "C" pkv_status pkv_create(const pkv_config *cfg, pkv_handle_t *out) {
     if (c.sink_page >= c.num_cache_pages)
         return fail(nullptr, PKV_ERR_INVALID, "sink_page outside the cache");
     if (c.graph_static != 0 && c.graph_static != 1) return fail(nullptr, PKV_ERR_INVALID, "graph_static is 0 or 1");
+    if (c.enable_nvtx != 0 && c.enable_nvtx != 1) return fail(nullptr, PKV_ERR_INVALID, "enable_nvtx is 0 or 1");
     if ((long long)c.num_cache_pages * 2 * c.page_size >= (1ll << 31))
         return fail(nullptr, PKV_ERR_UNSUPPORTED, "cache has too many pages for 32-bit slot rows");
     int sms = c.sm_count;
@@ -86,6 +101,7 @@ extern "C" pkv_status pkv_create(const pkv_config *cfg, pkv_handle_t *out) {
     h->shape = Shape{c.num_qo_heads, c.num_kv_heads, c.head_dim,       c.page_size, c.max_batch,
                      c.max_total_tokens, c.max_num_pages, c.num_cache_pages, c.max_prefill_rows,
                      sms,             c.sink_page,      c.graph_static};
+    h->nvtx = c.enable_nvtx != 0;
     *out = h;
     return PKV_OK;
 }
@@ -165,6 +181,7 @@ extern "C" pkv_status pkv_plan(pkv_handle_t h, int mode, const int32_t *qo_indpt
                                const int32_t *kv_indices, const int32_t *last_page_len, int batch, int causal,
                                int window_left, float sm_scale, void *workspace, size_t workspace_bytes,
                                pkv_stream_t stream) {
+    NvtxCall nvtx_range(h, "pkv_plan");
     if (!h) return fail(h, PKV_ERR_INVALID, "null handle");
     if (!workspace) return fail(h, PKV_ERR_INVALID, "null workspace");
     if (reinterpret_cast<uintptr_t>(workspace) % pkv::kAlign)
@@ -279,6 +296,7 @@ static pkv_status pf_map(pkv_handle_t h, const void *kv) {
 
 extern "C" pkv_status pkv_kv_append(pkv_handle_t h, const void *k, const void *v, void *kv_layer, void *workspace,
                                     pkv_stream_t stream) {
+    NvtxCall nvtx_range(h, "pkv_kv_append");
     pkv_status st = check_planned(h, workspace, PKV_MODE_DECODE, PKV_MODE_PREFILL);
     if (st != PKV_OK && h && h->plan.mode == PKV_MODE_MIXED && h->planned_ws == workspace) st = PKV_OK;
     if (st != PKV_OK) return st;
@@ -298,6 +316,7 @@ static pkv_status check_io(pkv_handle_t h, const void *q, const void *kv, void *
 
 extern "C" pkv_status pkv_run_decode(pkv_handle_t h, const void *q, const void *kv_layer, void *out, float *lse,
                                      void *workspace, pkv_stream_t stream) {
+    NvtxCall nvtx_range(h, "pkv_run_decode");
     pkv_status st = check_planned(h, workspace, PKV_MODE_DECODE);
     if (st != PKV_OK) return st;
     if (h->plan.batch == 0) return PKV_OK;
@@ -311,6 +330,7 @@ extern "C" pkv_status pkv_run_decode(pkv_handle_t h, const void *q, const void *
 extern "C" pkv_status pkv_run_decode_append(pkv_handle_t h, const void *q, const void *k, const void *v,
                                             void *kv_layer, void *out, float *lse, void *workspace,
                                             pkv_stream_t stream) {
+    NvtxCall nvtx_range(h, "pkv_run_decode_append");
     pkv_status st = check_planned(h, workspace, PKV_MODE_DECODE);
     if (st != PKV_OK) return st;
     if (h->plan.batch == 0) return PKV_OK;
@@ -326,6 +346,7 @@ extern "C" pkv_status pkv_run_decode_append(pkv_handle_t h, const void *q, const
 
 extern "C" pkv_status pkv_run_prefill(pkv_handle_t h, const void *q, const void *kv_layer, void *out, float *lse,
                                       void *workspace, pkv_stream_t stream) {
+    NvtxCall nvtx_range(h, "pkv_run_prefill");
     pkv_status st = check_planned(h, workspace, PKV_MODE_PREFILL);
     if (st != PKV_OK) return st;
     if (h->plan.num_tokens == 0) return PKV_OK;
@@ -339,6 +360,7 @@ extern "C" pkv_status pkv_run_prefill(pkv_handle_t h, const void *q, const void 
 
 extern "C" pkv_status pkv_run_mixed(pkv_handle_t h, const void *q, const void *kv_layer, void *out, float *lse,
                                     void *workspace, pkv_stream_t stream) {
+    NvtxCall nvtx_range(h, "pkv_run_mixed");
     pkv_status st = check_planned(h, workspace, PKV_MODE_MIXED);
     if (st != PKV_OK) return st;
     if (h->plan.num_tokens == 0) return PKV_OK;
@@ -370,6 +392,7 @@ extern "C" pkv_status pkv_run_mixed(pkv_handle_t h, const void *q, const void *k
 }
 
 extern "C" pkv_status pkv_check_device_error(pkv_handle_t h, void *workspace, pkv_stream_t stream, int *code) {
+    NvtxCall nvtx_range(h, "pkv_check_device_error");
     if (!h || !workspace || !code) return fail(h, PKV_ERR_INVALID, "null argument");
     if (h->planned_ws != workspace) return fail(h, PKV_ERR_NOT_PLANNED, "no plan on this workspace");
     int v = 0;
@@ -390,6 +413,7 @@ extern "C" pkv_status pkv_check_device_error(pkv_handle_t h, void *workspace, pk
 }
 
 extern "C" pkv_status pkv_selftest_wait_timeout(pkv_handle_t h, void *workspace, int polls, pkv_stream_t stream) {
+    NvtxCall nvtx_range(h, "pkv_selftest_wait_timeout");
     if (!h || !workspace) return fail(h, PKV_ERR_INVALID, "null argument");
     if (polls < 1 || polls > (1 << 20)) return fail(h, PKV_ERR_INVALID, "polls must be in [1, 2^20]");
     if (h->planned_ws != workspace) return fail(h, PKV_ERR_NOT_PLANNED, "no plan on this workspace");
@@ -444,6 +468,7 @@ extern "C" pkv_status pkv_mixed_layout(const int32_t *qo, const int32_t *kvp, co
 
 extern "C" pkv_status pkv_decode_split(pkv_handle_t h, const int32_t *kvp, const int32_t *lpl, int batch,
                                        int window_left, int32_t *tiles, int *num_tiles, int *num_ctas) {
+    NvtxCall nvtx_range(h, "pkv_decode_split");
     if (!h || !kvp || !lpl || !tiles || !num_tiles || !num_ctas || batch < 0) return PKV_ERR_INVALID;
     std::vector<int32_t> qt(batch), ot(batch);
     for (int r = 0; r < batch; ++r) qt[r] = ot[r] = r;
@@ -474,6 +499,7 @@ extern "C" pkv_status pkv_run_decode_static(pkv_handle_t h, const void *q, const
                                             float *lse, const int32_t *kv_indptr, const int32_t *kv_indices,
                                             const int32_t *last_page_len, int batch, int window_left, float sm_scale,
                                             pkv_stream_t stream) {
+    NvtxCall nvtx_range(h, "pkv_run_decode_static");
     if (!h) return fail(h, PKV_ERR_INVALID, "null handle");
     if (!(sm_scale >= 0.f) || std::isinf(sm_scale)) return fail(h, PKV_ERR_INVALID, "sm_scale must be finite and >= 0");
     std::string err;
@@ -506,6 +532,7 @@ extern "C" pkv_status pkv_run_decode_static(pkv_handle_t h, const void *q, const
 extern "C" pkv_status pkv_plan_dense(pkv_handle_t h, const int32_t *cu_q, const int32_t *cu_k, int batch, int causal,
                                      int window_left, float sm_scale, void *workspace, size_t workspace_bytes,
                                      pkv_stream_t stream) {
+    NvtxCall nvtx_range(h, "pkv_plan_dense");
     if (!h) return fail(h, PKV_ERR_INVALID, "null handle");
     if (!workspace) return fail(h, PKV_ERR_INVALID, "null workspace");
     if (reinterpret_cast<uintptr_t>(workspace) % pkv::kAlign)
@@ -521,6 +548,7 @@ extern "C" pkv_status pkv_plan_dense(pkv_handle_t h, const int32_t *cu_q, const 
 
 extern "C" pkv_status pkv_run_dense(pkv_handle_t h, const void *q, const void *k, const void *v, void *out, float *lse,
                                     void *workspace, pkv_stream_t stream) {
+    NvtxCall nvtx_range(h, "pkv_run_dense");
     pkv_status st = check_planned(h, workspace, PKV_MODE_DENSE);
     if (st != PKV_OK) return st;
     if (h->plan.num_tokens == 0) return PKV_OK;
@@ -538,6 +566,7 @@ extern "C" pkv_status pkv_run_dense(pkv_handle_t h, const void *q, const void *k
 
 extern "C" pkv_status pkv_gather_kv(pkv_handle_t h, const void *kv_layer, const int32_t *pages, int num_tokens,
                                     void *k_out, void *v_out, pkv_stream_t stream) {
+    NvtxCall nvtx_range(h, "pkv_gather_kv");
     if (!h) return fail(h, PKV_ERR_INVALID, "null handle");
     if (num_tokens < 0) return fail(h, PKV_ERR_INVALID, "num_tokens must be >= 0");
     if (num_tokens == 0) return PKV_OK;

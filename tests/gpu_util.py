@@ -19,12 +19,12 @@ LSE_REL = 1e-3
 MODES = {"decode": B.MODE_DECODE, "prefill": B.MODE_PREFILL, "mixed": B.MODE_MIXED}
 
 
-def make_handle(pb, *, sm_count=0, max_prefill_rows=None):
+def make_handle(pb, *, sm_count=0, max_prefill_rows=None, enable_nvtx=False):
     mpr = pb.max_prefill_rows if max_prefill_rows is None else max_prefill_rows
     return B.Handle(num_qo_heads=pb.num_qo_heads, num_kv_heads=pb.num_kv_heads, head_dim=pb.head_dim,
                     page_size=pb.page_size, max_batch=max(pb.batch, 1), max_total_tokens=max(pb.num_tokens, 1),
                     max_num_pages=max(len(pb.kv_indices), 1), num_cache_pages=pb.max_pages,
-                    max_prefill_rows=mpr, sm_count=sm_count, sink_page=pb.sink_page)
+                    max_prefill_rows=mpr, sm_count=sm_count, sink_page=pb.sink_page, enable_nvtx=enable_nvtx)
 
 
 def gpu_step(pb, x, mode, *, layer=0, window_left=-1, causal=True, sm_scale=0.0, sm_count=0, append=True,

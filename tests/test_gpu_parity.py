@@ -267,6 +267,23 @@ def test_repeated_runs_are_bit_identical(mode):
         assert torch.equal(lse, lse0)
 
 
+@pytest.mark.parametrize("mode", ["decode", "prefill", "mixed"])
+def test_nvtx_handle_gives_bit_identical_results(mode):
+    """A handle made with enable_nvtx (one NVTX range per call) computes exactly what a
+    handle without it computes: plan, append and run on copies of the same inputs."""
+    n = [1, 1, 300, 1, 77] if mode == "mixed" else ([1] * 5 if mode == "decode" else [40, 3, 300, 9, 77])
+    c = [900, 40, 20, 2000, 300]
+    pb = _mixed_batch(44, n, c) if mode == "mixed" else wl.custom(44, np.add(n, c), n, num_qo_heads=32,
+                                                                  num_kv_heads=8, head_dim=128, page_size=16)
+    res = []
+    for nvtx in (False, True):
+        x = wl.make_inputs(pb, device="cuda", seed=14, unused="nan", layers=1)
+        h = G.make_handle(pb, enable_nvtx=nvtx)
+        out, lse, _, _ = G.gpu_step(pb, x, mode, handle=h)
+        res.append((out.view(torch.int16).clone(), lse.clone(), x["kv_cache"][0].view(torch.int16).clone()))
+    assert torch.equal(res[0][0], res[1][0]) and torch.equal(res[0][1], res[1][1]) and torch.equal(res[0][2], res[1][2])
+
+
 # ------------------------------------------------------------------ context-only attention (causal = 2)
 
 @pytest.mark.parametrize("window", [-1, 0, 5, 100])

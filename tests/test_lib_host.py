@@ -51,6 +51,7 @@ def _handle(**kw):
     (dict(num_kv_heads=1, num_qo_heads=9), B.ERR_UNSUPPORTED),
     (dict(max_batch=0), B.ERR_INVALID),
     (dict(sink_page=200000), B.ERR_INVALID),
+    (dict(enable_nvtx=2), B.ERR_INVALID),
 ])
 def test_create_rejects(lib, kw, status):
     with pytest.raises(B.PkvError) as e:
@@ -149,6 +150,20 @@ def test_decode_split_covers_each_visible_page_once(lib, name, window, P, Hkv):
             assert np.all(mine[:, 3] >= 0)
     parts = tiles[tiles[:, 3] >= 0, 3]
     assert sorted(parts.tolist()) == list(range(len(parts)))
+
+
+def test_nvtx_ranges_leave_host_results_unchanged(lib):
+    """enable_nvtx (the wrappers' constructor flag) only opens a range per call: the split
+    and a plan rejected before any copy come out the same, and a range opened by a call
+    that returns early is closed (the next calls still work)."""
+    pb = _split_case("batch", 16)
+    on, off = (_handle(num_cache_pages=pb.max_pages, enable_nvtx=f) for f in (True, False))
+    for _ in range(3):
+        t_on, c_on = on.decode_split(pb.kv_indptr, pb.last_page_len, -1)
+        t_off, c_off = off.decode_split(pb.kv_indptr, pb.last_page_len, -1)
+        assert c_on == c_off and np.array_equal(t_on, t_off)
+        bad = ([0, 1], [0, 2, 1], [0, 1], [1, 1])  # kv_indptr decreases
+        assert _plan_status(on, B.MODE_DECODE, (None,) + bad[1:]) == _plan_status(off, B.MODE_DECODE, (None,) + bad[1:])
 
 
 def _plan_status(h, mode, idx, **kw):
