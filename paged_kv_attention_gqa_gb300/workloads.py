@@ -183,7 +183,7 @@ def custom(seed: int, kv_lens, qo_lens, *, num_qo_heads, num_kv_heads, head_dim,
                       sink_page=sink, **kw)
 
 
-CONFIGS = {
+WORKLOADS = {
     "tiny": config_tiny,
     "batch": config_batch_decode,
     "prefill": config_prefill,

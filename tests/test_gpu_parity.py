@@ -195,7 +195,7 @@ def test_mixed_poisoned_sink_rows_do_not_leak():
     _check_step(pb, "mixed", seed=11)
 
 
-# ------------------------------------------------------------------ full-size configs (launch config of bench.py)
+# ------------------------------------------------------------------ full-size workloads (launch configuration of bench.py)
 
 def test_batch_decode_full_size():
     pb = wl.config_batch_decode()

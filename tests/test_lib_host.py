@@ -76,7 +76,7 @@ def test_golden_mixed_layout(lib):
 
 @pytest.mark.parametrize("name", ["tiny", "batch", "prefill", "mixed", "long"])
 def test_planner_matches_oracle_index_work(lib, name):
-    pb = wl.CONFIGS[name]()
+    pb = wl.WORKLOADS[name]()
     idx = pb.index_arrays()
     a = B.append_slots(pb.page_size, *idx)
     b = plan_ref.append_slots(*idx, pb.page_size)
@@ -116,9 +116,9 @@ def test_too_many_prompt_rows_status(lib):
 
 def _split_case(name, P):
     if P == 16:
-        return wl.CONFIGS[name]()
+        return wl.WORKLOADS[name]()
     # the same lengths on pages of P slots
-    base = wl.CONFIGS[name]()
+    base = wl.WORKLOADS[name]()
     return wl.custom(7, base.kv_lens, base.qo_lens, num_qo_heads=base.num_qo_heads, num_kv_heads=base.num_kv_heads,
                      head_dim=base.head_dim, page_size=P)
 
@@ -217,7 +217,7 @@ def test_plan_validation(lib, case, status):
 
 def test_workspace_bound_holds(lib):
     for name in ["tiny", "batch", "prefill", "mixed", "long"]:
-        pb = wl.CONFIGS[name]()
+        pb = wl.WORKLOADS[name]()
         h = _handle(num_qo_heads=pb.num_qo_heads, num_kv_heads=pb.num_kv_heads, head_dim=pb.head_dim,
                     max_batch=pb.batch, max_total_tokens=max(pb.num_tokens, pb.batch),
                     max_num_pages=len(pb.kv_indices), num_cache_pages=pb.max_pages,
