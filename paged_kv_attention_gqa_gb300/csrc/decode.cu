@@ -206,9 +206,10 @@ __global__ void __launch_bounds__((D > 128 ? 4 + (SMALL ? 2 : 1) : 8 + (SMALL ? 
                     const int pos = pos0 + kslot + KPI * i;
                     row[i] = pos < cr.end ? a.pages[t.kv_base + (pos >> a.page_shift)] * 2 * P + (pos & (P - 1)) : -1;
                 }
-                bool w = true;
-                if (lane == 0 && use > 0) w = mbar_wait(&empty[s], (use - 1) & 1, err, kErrWaitEmpty);
-                if (!__shfl_sync(0xffffffffu, w ? 1 : 0, 0)) {
+                // every lane waits on the barrier itself (they wake together); the vote keeps
+                // the warp on one path if a wait gives up
+                const bool w = use == 0 || mbar_wait(&empty[s], (use - 1) & 1, err, kErrWaitEmpty);
+                if (!__all_sync(0xffffffffu, w)) {
                     ok = false;
                     break;
                 }

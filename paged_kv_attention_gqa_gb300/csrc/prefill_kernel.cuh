@@ -262,11 +262,11 @@ __global__ void __launch_bounds__(GATHER ? kPfGatherThreads : kPfThreads, D > 12
                     const int pos = key0 + kslot + KPI * (pw + kPfGatherWarps * i);
                     row[i] = pos < t.length ? a.pages[t.kv_base + (pos >> a.page_shift)] * 2 * P + (pos & (P - 1)) : -1;
                 }
-                bool ok = true;
-                if (lane == 0 && use > 0)
-                    ok = mbar_wait(&s_full[s], (use - 1) & 1, err, kErrWaitEmpty) &&
-                         mbar_wait(&pv_done[s], (use - 1) & 1, err, kErrWaitEmpty);
-                if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+                // every lane waits on the barriers itself (they wake together); the vote keeps
+                // the warp on one path if a wait gives up
+                const bool ok = use == 0 || (mbar_wait(&s_full[s], (use - 1) & 1, err, kErrWaitEmpty) &&
+                                             mbar_wait(&pv_done[s], (use - 1) & 1, err, kErrWaitEmpty));
+                if (!__all_sync(0xffffffffu, ok)) break;
                 const uint32_t kd = smem_u32(sm + L::K_OFF + s * L::KV_BYTES) + (c >> 3) * (L::KV_BYTES / HALVES);
                 const uint32_t vd = smem_u32(sm + L::V_OFF + s * L::KV_BYTES) + (c >> 3) * (L::KV_BYTES / HALVES);
 #pragma unroll
