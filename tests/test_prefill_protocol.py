@@ -16,6 +16,9 @@ Checked under many random schedules (any issue, load, MMA and wake-up latency):
     softmax reads S_j only after it completed; PV_j is issued only after P_j was written and
     V_j landed; O is rescaled only while no PV is in flight; the epilogue reads O after all PVs;
   * every actor finishes (no deadlock).
+The same holds for the cp.async gather path (pages below 8 slots): four producer warps, each
+waiting on both barriers of a slot, copying its share of the tile's K and V rows, and arriving
+on k_full / v_full, which then count four arrivals.
 A planted mistake (the MMA thread not waiting for PV_{j-2}, or the producer reusing a V slot
 on S-done) is caught, so the model can tell a broken protocol from a sound one."""
 import heapq
@@ -41,14 +44,15 @@ class Barrier:
 
 
 class Sim:
-    def __init__(self, nt, seed, plant=None):
+    def __init__(self, nt, seed, plant=None, gather=False):
         self.rng = random.Random(seed)
-        self.nt, self.plant = nt, plant
+        self.nt, self.plant, self.gather = nt, plant, gather
+        nfull = 4 if gather else 1
         self.t, self.seq, self.q = 0, 0, []
         B = Barrier
         self.q_full = B("q_full", 1)
-        self.k_full = [B(f"k_full{s}", 1) for s in range(2)]
-        self.v_full = [B(f"v_full{s}", 1) for s in range(2)]
+        self.k_full = [B(f"k_full{s}", nfull) for s in range(2)]
+        self.v_full = [B(f"v_full{s}", nfull) for s in range(2)]
         self.s_full = [B(f"s_full{s}", 1) for s in range(2)]
         self.p_full = [B(f"p_full{s}", 4) for s in range(2)]
         self.pv_done = [B(f"pv_done{s}", 1) for s in range(2)]
@@ -128,6 +132,27 @@ class Sim:
                 raise AssertionError(f"V slot of tile {j} reused before PV_{j - 2} done")
             self.tma(self.v_full[s], self.v_load, j)
 
+    def gather_producer(self, w):
+        # one of four cp.async producer warps: waits on both barriers of the slot, copies its
+        # share of tile j's K and V rows, waits for its copies, arrives on both full barriers
+        for j in range(self.nt):
+            s, use = j & 1, j >> 1
+            if use > 0:
+                yield ("wait", self.s_full[s], use - 1)
+                if self.plant == "v_slot_on_s_done":
+                    yield ("wait", self.s_full[s], use - 1)
+                else:
+                    yield ("wait", self.pv_done[s], use - 1)
+            if j >= 2 and self.s_cpl.get(j - 2, float("inf")) > self.t:
+                raise AssertionError(f"K slot of tile {j} overwritten before S_{j - 2} done")
+            if j >= 2 and self.pv_cpl.get(j - 2, float("inf")) > self.t:
+                raise AssertionError(f"V slot of tile {j} overwritten before PV_{j - 2} done")
+            yield ("delay", self.rng.randint(50, 2500))  # issue, then wait for its own copies
+            self.k_land[j] = max(self.k_land.get(j, 0), self.t)
+            self.v_land[j] = max(self.v_land.get(j, 0), self.t)
+            self.k_full[s].arrive(self)
+            self.v_full[s].arrive(self)
+
     def mma(self):
         yield ("wait", self.q_full, 0)
 
@@ -175,7 +200,12 @@ class Sim:
         assert len(self.pv_cpl) == self.nt and max(self.pv_cpl.values(), default=0) <= self.t
 
     def run(self):
-        actors = [self.producer(), self.mma()] + [self.softmax(w) for w in range(4)]
+        if self.gather:
+            self.q_full.arrive(self)
+            producers = [self.gather_producer(w) for w in range(4)]
+        else:
+            producers = [self.producer()]
+        actors = producers + [self.mma()] + [self.softmax(w) for w in range(4)]
         for a in actors:
             self.run_actor(a)
         while self.q:
@@ -184,18 +214,22 @@ class Sim:
         assert self.finished == len(actors), f"deadlock: {self.finished} of {len(actors)} actors finished"
 
 
+@pytest.mark.parametrize("gather", [False, True])
 @pytest.mark.parametrize("nt", [1, 2, 3, 4, 5, 8, 13])
-def test_prefill_barrier_protocol_is_sound(nt):
+def test_prefill_barrier_protocol_is_sound(nt, gather):
     for seed in range(150):
-        Sim(nt, seed * 1000 + nt).run()
+        Sim(nt, seed * 1000 + nt, gather=gather).run()
 
 
-@pytest.mark.parametrize("plant", ["no_pv_wait", "v_slot_on_s_done"])
-def test_model_catches_a_broken_protocol(plant):
+# In the gather path the producers already wait for PV_{j-2} before copying K_j, so there the
+# MMA thread's own wait for it is redundant and dropping it breaks nothing.
+@pytest.mark.parametrize("plant,gather", [("no_pv_wait", False), ("v_slot_on_s_done", False),
+                                          ("v_slot_on_s_done", True)])
+def test_model_catches_a_broken_protocol(plant, gather):
     caught = 0
     for seed in range(200):
         try:
-            Sim(8, seed, plant=plant).run()
+            Sim(8, seed, plant=plant, gather=gather).run()
         except AssertionError:
             caught += 1
     assert caught > 0
