@@ -64,3 +64,46 @@ def test_mutant_is_caught(name, tmp_path):
         except (AssertionError, ValueError, IndexError) as e:
             caught.append(pin.__name__)
     assert caught, f"no pin caught mutation {name}"
+
+
+# ---- the index oracle (oracle/plan_ref.py): mistakes planted in a copy of its source ----
+
+import importlib.util  # noqa: E402
+
+import plan_pins  # noqa: E402
+from oracle import plan_ref  # noqa: E402
+
+PLAN_SRC = open(plan_ref.__file__).read()
+
+PLAN_MUTATIONS = {
+    # context_only_views keeps the LAST pages of a row instead of the first
+    "context_only_keeps_last_pages": ("new_i.extend(int(x) for x in kvi[kvp[r]: kvp[r] + keep])",
+                                      "new_i.extend(int(x) for x in kvi[kvp[r + 1] - keep: kvp[r + 1]])"),
+    # ... keeps one page too many when the context ends on a page boundary
+    "context_only_extra_page": ("keep = -(-ctx // page_size)", "keep = ctx // page_size + 1 if ctx else 0"),
+    # ... leaves the last page's fill as it was
+    "context_only_fill_unchanged": ("new_l.append(last_page_len_of(ctx, page_size) if ctx > 0 else 0)",
+                                    "new_l.append(int(last_page_len[r]) if ctx > 0 else 0)"),
+    "append_slot_one_late": ("p = c + i\n            pages[qo[r] + i]", "p = c + i + 1\n            pages[qo[r] + i]"),
+    "append_row_start_position": ("c = int(L[r]) - n\n", "c = 0\n"),
+    "perm_prompt_rows_reversed": ("for r in prompt:\n        perm.extend", "for r in prompt[::-1]:\n        perm.extend"),
+    "sink_row_keeps_pages": ("dec_kvi.append(int(sink_page))", "dec_kvi.extend(int(x) for x in kvi[kvp[r]: kvp[r + 1]])"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PLAN_MUTATIONS))
+def test_plan_mutant_is_caught(name, tmp_path):
+    old, new = PLAN_MUTATIONS[name]
+    assert PLAN_SRC.count(old) == 1, f"mutation anchor for {name} not found"
+    path = tmp_path / f"plan_ref_{name}.py"
+    path.write_text(PLAN_SRC.replace(old, new))
+    spec = importlib.util.spec_from_file_location(f"plan_ref_{name}", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    caught = []
+    for pin in plan_pins.ALL_PLAN_PINS:
+        try:
+            pin(mod)
+        except (AssertionError, ValueError, IndexError) as e:
+            caught.append(pin.__name__)
+    assert caught, f"no pin caught mutation {name}"

@@ -1,34 +1,22 @@
 """The oracle's index work against a hand-worked layout and against brute-force
 properties (CPU only)."""
-import json
-import os
-
 import numpy as np
 import pytest
 
 from oracle import plan_ref
+import plan_pins
 from paged_kv_attention_gqa_gb300 import workloads as wl
 
-GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "mixed_layout.json")))
+GOLD = plan_pins.MIXED
 
 
 def _idx(g):
     return g["qo_indptr"], g["kv_indptr"], g["kv_indices"], g["last_page_len"]
 
 
-def test_golden_append_slots():
-    ex = GOLD["expect"]
-    assert plan_ref.row_lengths(GOLD["kv_indptr"], GOLD["last_page_len"], 16).tolist() == ex["row_lengths"]
-    pages, slots = plan_ref.append_slots(*_idx(GOLD), 16)
-    assert pages.tolist() == ex["append_pages"]
-    assert slots.tolist() == ex["append_slots"]
-
-
-def test_golden_mixed_layout():
-    lay = plan_ref.mixed_layout(*_idx(GOLD), max_prefill_rows=GOLD["max_prefill_rows"], sink_page=GOLD["sink_page"])
-    for key, want in GOLD["expect"].items():
-        if key in lay:
-            assert lay[key].tolist() == want, key
+@pytest.mark.parametrize("pin", plan_pins.ALL_PLAN_PINS, ids=lambda f: f.__name__)
+def test_plan_pin(pin):
+    pin()
 
 
 def test_too_many_prompt_rows():
