@@ -7,7 +7,7 @@ Default workload: batch decode, 128 requests, 32 q heads / 8 kv heads, head_dim 
 page_size 16, kv lengths U[512, 4096] (seed 0), a 32-layer cache
 [32, pages, 2, 16, 8, 128] bf16 of 42.7 GB.  One step = plan (host) + for each of the
 32 layer slices: last-page append and batched decode, in one launch
-(pkv_run_decode_append; --separate-append issues pkv_kv_append + pkv_run_decode).  The
+(pkv_run_decode_append; --separate-append issues pkv_kv_append_planned + pkv_run_decode).  The
 metric is KV GB/s: the K and V bytes of every visible token per layer, over the device
 time of the step.
 The cache streamed per step is far larger than L2, so no flush is needed.
@@ -53,7 +53,7 @@ def parse():
     ap.add_argument("--no-secondary", action="store_true", help="skip the prefill / mixed / long-decode lines")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--separate-append", action="store_true",
-                    help="decode workloads: pkv_kv_append + pkv_run_decode per layer instead of the fused call")
+                    help="decode workloads: pkv_kv_append_planned + pkv_run_decode per layer instead of the fused call")
     ap.add_argument("--layers", type=int, default=0, help="fewer cache layers (profiling a small case)")
     return ap.parse_args()
 
@@ -242,7 +242,7 @@ def run_ours(args, rank, world):
 
     def layer(l, q, k, v, o, ls):
         if args.separate_append:
-            h.kv_append(k, v, cache[l], workspace=ws)
+            h.kv_append_planned(k, v, cache[l], workspace=ws)
             h.run_decode(q, cache[l], o, ls, workspace=ws)
         else:
             h.run_decode_append(q, k, v, cache[l], o, ls, workspace=ws)
@@ -371,7 +371,7 @@ def run_ours(args, rank, world):
         "config": {"workload": f"{pb.name}: {pb.batch} requests, Hq {pb.num_qo_heads} / Hkv {pb.num_kv_heads}, "
                                f"head_dim {pb.head_dim}, page_size {pb.page_size}, {L} layers, window_left {window}",
                    "kv_cache_bytes": int(cache.numel() * 2), "kv_bytes_per_step": int(step_bytes),
-                   "step": (f"plan + {L} x (pkv_kv_append + pkv_run_decode)" if args.separate_append else
+                   "step": (f"plan + {L} x (pkv_kv_append_planned + pkv_run_decode)" if args.separate_append else
                             f"plan + {L} x pkv_run_decode_append (append fused into the decode launch)"),
                    "l2": "inputs larger than L2: every step streams the whole cache",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
@@ -423,7 +423,7 @@ def run_step_primary(args, rank, world):
         flush()
         a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
         a.record(stream)
-        h.kv_append(x["k_new"], x["v_new"], kv, workspace=ws)
+        h.kv_append_planned(x["k_new"], x["v_new"], kv, workspace=ws)
         b.record(stream)
         run(x["q"], kv, out, lse, workspace=ws)
         c.record(stream)
@@ -510,9 +510,9 @@ def secondary(B, dev, peaks, seed):
     kv = x["kv_cache"][0]
     out = torch.empty_like(x["q"])
     lse = torch.empty(x["q"].shape[:2], dtype=torch.float32, device=dev)
-    h.kv_append(x["k_new"], x["v_new"], kv, workspace=ws)
+    h.kv_append_planned(x["k_new"], x["v_new"], kv, workspace=ws)
     ms = time_runs(lambda: h.run_prefill(x["q"], kv, out, lse, workspace=ws), flush)
-    app_ms = time_runs(lambda: h.kv_append(x["k_new"], x["v_new"], kv, workspace=ws), flush)
+    app_ms = time_runs(lambda: h.kv_append_planned(x["k_new"], x["v_new"], kv, workspace=ws), flush)
     fl = prefill_flops(pb)
     tf = fl / (ms * 1e-3) / 1e12
     res["prefill"] = {"workload": "16 rows, new U[128,2048], prefix U[0,4096], 32/8/128, causal",
@@ -532,7 +532,7 @@ def secondary(B, dev, peaks, seed):
     kv = x["kv_cache"][0]
     out = torch.empty_like(x["q"])
     lse = torch.empty(x["q"].shape[:2], dtype=torch.float32, device=dev)
-    h.kv_append(x["k_new"], x["v_new"], kv, workspace=ws)
+    h.kv_append_planned(x["k_new"], x["v_new"], kv, workspace=ws)
     ms = time_runs(lambda: h.run_mixed(x["q"], kv, out, lse, workspace=ws), flush)
     dec = [r for r in range(pb.batch) if pb.qo_lens[r] == 1]
     dec_bytes = sum(int(pb.kv_lens[r]) for r in dec) * pb.num_kv_heads * pb.head_dim * 4

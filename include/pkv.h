@@ -29,10 +29,14 @@
  * window_left is the number of preceding positions a query sees, -1 unbounded);
  *   out = softmax(sm_scale * q K^T) V (bf16), lse = natural-log log-sum-exp (fp32).
  *
- * Call order for one step:  pkv_plan (host)  ->  per layer: pkv_kv_append, then
- * pkv_run_decode / pkv_run_prefill / pkv_run_mixed.  One plan serves every layer
- * until the next plan on that workspace (DensePlan: "once per step and read by each
- * layer run").  run and append calls allocate nothing and never synchronise the host.
+ * Call order for one step:  pkv_plan (host)  ->  per layer: pkv_kv_append (or
+ * pkv_kv_append_planned), then pkv_run_decode / pkv_run_prefill / pkv_run_mixed.  One
+ * plan serves every layer until the next plan on that workspace (DensePlan: "once per
+ * step and read by each layer run").  run and append calls allocate nothing and never
+ * synchronise the host.  A plan reaches its workspace through a copy queued on the
+ * plan's stream, so the runs and appends that read it must be queued on that stream, or
+ * on one ordered after it (an event); the next plan on the same workspace overwrites it
+ * in stream order, so plans may run ahead of the GPU on one stream.
  *
  * Errors: every function returns a pkv_status; validation happens on the host before
  * any launch; pkv_last_error() explains the last failure.  Kernels never trap: a
@@ -85,8 +89,9 @@ enum { PKV_NON_CAUSAL = 0, PKV_CAUSAL = 1, PKV_CONTEXT_ONLY = 2 };
  *   graph_static:     1 = CUDA-graph mode (the wrappers' accelerator_graph): every plan
  *                     uses the workspace layout of the handle's maxima and every kernel is
  *                     launched at the maxima, reading the plan's own counts, causal flag,
- *                     window and scale from the workspace.  pkv_kv_append / pkv_run_* calls
- *                     captured once into a CUDA graph then stay valid for every later
+ *                     window and scale from the workspace.  pkv_kv_append_planned /
+ *                     pkv_run_* calls captured once into a CUDA graph then stay valid for
+ *                     every later
  *                     pkv_plan on the same workspace, as long as q, out, lse, k, v and the
  *                     layer slices keep their addresses and q / out / k / v are sized for
  *                     the maxima (max_batch rows for decode, max_total_tokens otherwise).
@@ -156,7 +161,7 @@ pkv_status pkv_workspace_size(pkv_handle_t h, int mode, size_t *bytes);
  *                 pkv_context_only_views), query i of row r sits at position L_r + i and
  *                 sees every context key (window_left counted from that position); n_r may
  *                 exceed L_r; a query that sees no key gets out = 0 and lse = -inf.  Such a
- *                 plan appends nothing (pkv_kv_append is a no-op on it).
+ *                 plan appends nothing (pkv_kv_append_planned is a no-op on it).
  *   window_left   -1 unbounded, else >= 0.
  *   sm_scale      0 selects 1/sqrt(head_dim).
  *   workspace     device buffer of workspace_bytes (>= pkv_workspace_size for the
@@ -171,13 +176,44 @@ pkv_status pkv_plan(pkv_handle_t h, int mode, const int32_t *qo_indptr, const in
                     pkv_stream_t stream);
 
 /*
- * Last-page KV append (the write locations the plan computed; the KVManager's write
- * before attention).  k, v: device bf16 [T, num_kv_heads, head_dim], T = the planned
- * step's new tokens (decode: batch).  kv_layer: device layer slice, written in place
- * at (page, slot) of each new token; nothing else in the slice is touched.
+ * Last-page KV append from the index arrays themselves (the KVManager's write before
+ * attention: DenseAttentionManager.requires_kv_write; the write location of
+ * FlashInferDecodeWrapper.plan).  No plan is needed.  New token t of row r (qo_indptr[r]
+ * <= t < qo_indptr[r+1]) sits at position p = L_r - n_r + (t - qo_indptr[r]) of the
+ * post-append row and is written to page paged_kv_indices[paged_kv_indptr[r] + p /
+ * page_size], slot p % page_size: its K row to [page, 0, slot, :, :] and its V row to
+ * [page, 1, slot, :, :] of the layer slice.  Nothing else in the slice is touched.
+ *   k, v:           DEVICE bf16 [num_new_tokens, num_kv_heads, head_dim], 16-byte aligned.
+ *   num_new_tokens: qo_indptr[batch] (batch when qo_indptr is NULL).
+ *   kv_layer:       DEVICE layer slice, written in place.
+ *   qo_indptr, paged_kv_indptr, paged_kv_indices, paged_kv_last_page_len: DEVICE int32
+ *                   arrays of the post-append state, as in pkv_plan; qo_indptr may be
+ *                   NULL (decode: row r's one new token is token r).
+ *   batch:          rows (<= max_batch).
+ * The host never reads the device arrays, so the kernel checks every token's location
+ * before it writes: a token whose row is inconsistent (non-monotone offsets, a fill
+ * outside 1..page_size, a position outside the row, a page id outside the cache) is left
+ * unwritten, and nothing outside the listed buffers is read or written.  Host-validated
+ * appends come from pkv_plan + pkv_kv_append_planned.  Allocates nothing, never
+ * synchronises, so it can sit in a captured graph.  PKV_ERR_INVALID on null or misaligned
+ * pointers and negative sizes.
  */
-pkv_status pkv_kv_append(pkv_handle_t h, const void *k, const void *v, void *kv_layer, void *workspace,
-                         pkv_stream_t stream);
+pkv_status pkv_kv_append(pkv_handle_t h, const void *k, const void *v, int num_new_tokens, void *kv_layer,
+                         const int32_t *qo_indptr, const int32_t *paged_kv_indptr, const int32_t *paged_kv_indices,
+                         const int32_t *paged_kv_last_page_len, int batch, pkv_stream_t stream);
+
+/*
+ * The same append at the write locations the last pkv_plan on `workspace` computed and
+ * validated on the host (FlashInferDecodeWrapper.plan: "compute KV write locations").
+ * k, v: device bf16 [T, num_kv_heads, head_dim], T = the planned step's new tokens
+ * (decode: batch).  kv_layer: device layer slice, written in place at (page, slot) of
+ * each new token; nothing else in the slice is touched.  Must be issued on the stream the
+ * plan was made on (or one ordered after it): the plan's copy into the workspace is
+ * ordered only on that stream.  PKV_ERR_NOT_PLANNED without a plan on `workspace`; a
+ * context-only plan appends nothing.
+ */
+pkv_status pkv_kv_append_planned(pkv_handle_t h, const void *k, const void *v, void *kv_layer, void *workspace,
+                                 pkv_stream_t stream);
 
 /*
  * Batched decode (FlashInferDecodeWrapper.run).  q: device bf16 [batch, Hq, D];
@@ -187,7 +223,7 @@ pkv_status pkv_run_decode(pkv_handle_t h, const void *q, const void *kv_layer, v
                           void *workspace, pkv_stream_t stream);
 
 /*
- * pkv_kv_append followed by pkv_run_decode, in one kernel launch (same results, the
+ * pkv_kv_append_planned followed by pkv_run_decode, in one kernel launch (same results, the
  * appended slots bit-identical).  Decode plans only (PKV_ERR_NOT_PLANNED otherwise).
  * k, v: device bf16 [batch, num_kv_heads, head_dim], 16-byte aligned; the rest as
  * pkv_run_decode.  The CTA that reads a row's last page writes the row's new token
@@ -259,20 +295,23 @@ pkv_status pkv_selftest_wait_timeout(pkv_handle_t h, void *workspace, int polls,
  * Decode that needs no workspace: plan + pkv_run_decode in one call, with the plan and
  * the split-KV partials kept in a 16 MiB scratch array compiled into the library
  * (one per GPU that loads it, held until the process exits).  The pages have no
- * counterpart to this call; it exists for callers that are handed only their inputs,
- * outputs and a stream and may not allocate device memory themselves, e.g. code running
- * while a CUDA graph is being captured, plugin hooks of inference runtimes, or latency-
- * critical paths that must not enter an allocator that can synchronise or fail.
+ * counterpart to this call.  It is for callers that are handed only their inputs,
+ * outputs and a stream and may not allocate device memory themselves: plugin hooks of
+ * inference runtimes whose host owns every allocation, and latency-critical paths that
+ * must not enter an allocator that can synchronise the device or fail.
  *   q, out, lse, kv_layer: as pkv_run_decode.  kv_indptr, kv_indices, last_page_len:
  *   HOST int32 arrays as in pkv_plan (decode: one new token per row).
- * The call plans on the host (ordinary heap memory only), copies the plan from pageable
- * memory into the scratch on `stream` (so it may wait for work already queued there), and
- * launches the decode and merge kernels; it makes no device or page-locked allocation.  Its first call on a device resolves the
- * scratch's device address (once per device, with that device current): make that first
- * call before any stream capture.  A decode whose plan needs more than 16 MiB returns
- * PKV_ERR_WORKSPACE.  Every call shares the one array and overwrites it: calls that
- * overlap on the GPU (other streams or threads) race; calls on one stream do not.
- * Device-side wait errors are recorded in the scratch and are not reported.
+ * The call plans on the host (ordinary heap memory only), copies the plan from that
+ * pageable memory into the scratch on `stream` (so it may wait for work already queued
+ * there), and launches the decode and merge kernels; it makes no device or page-locked
+ * allocation.  The scratch's device address is resolved once per CUDA context, on the
+ * first call made with that device current (again after cudaDeviceReset).
+ * Errors: PKV_ERR_WORKSPACE when the decode's plan and partials need more than 16 MiB
+ * (pkv_last_error names the bytes); PKV_ERR_INVALID when `stream` is capturing, since
+ * the plan is copied from host memory the call frees before returning; otherwise as
+ * pkv_plan.  Every call shares the one array and overwrites it: calls that overlap on
+ * the GPU (other streams or threads) race; calls on one stream do not.  Device-side
+ * wait errors are recorded in the scratch and are not reported.
  */
 pkv_status pkv_run_decode_static(pkv_handle_t h, const void *q, const void *kv_layer, void *out, float *lse,
                                  const int32_t *paged_kv_indptr, const int32_t *paged_kv_indices,

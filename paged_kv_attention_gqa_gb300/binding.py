@@ -21,7 +21,7 @@ NON_CAUSAL, CAUSAL, CONTEXT_ONLY = 0, 1, 2
 STATUS_NAMES = ["OK", "INVALID", "UNSUPPORTED", "WORKSPACE", "TOO_MANY_PREFILL_ROWS", "NOT_PLANNED", "CUDA", "DEVICE"]
 
 # every symbol include/pkv.h declares
-EXPORTS = ["pkv_create", "pkv_destroy", "pkv_last_error", "pkv_workspace_size", "pkv_plan", "pkv_kv_append",
+EXPORTS = ["pkv_create", "pkv_destroy", "pkv_last_error", "pkv_workspace_size", "pkv_plan", "pkv_kv_append", "pkv_kv_append_planned",
            "pkv_run_decode", "pkv_run_prefill", "pkv_run_mixed", "pkv_check_device_error", "pkv_append_slots",
            "pkv_mixed_layout", "pkv_decode_split", "pkv_run_decode_static", "pkv_context_only_views",
            "pkv_plan_dense", "pkv_run_dense", "pkv_gather_kv", "pkv_run_decode_append", "pkv_selftest_wait_timeout"]
@@ -59,7 +59,8 @@ def load(path: str = LIB_PATH):
         "pkv_last_error": ([vp], ctypes.c_char_p),
         "pkv_workspace_size": ([vp, i, ctypes.POINTER(ctypes.c_size_t)], i),
         "pkv_plan": ([vp, i, i32p, i32p, i32p, i32p, i, i, i, ctypes.c_float, vp, ctypes.c_size_t, vp], i),
-        "pkv_kv_append": ([vp, vp, vp, vp, vp, vp], i),
+        "pkv_kv_append": ([vp, vp, vp, i, vp, vp, vp, vp, vp, i, vp], i),
+        "pkv_kv_append_planned": ([vp, vp, vp, vp, vp, vp], i),
         "pkv_run_decode": ([vp, vp, vp, vp, vp, vp, vp], i),
         "pkv_run_decode_append": ([vp, vp, vp, vp, vp, vp, vp, vp, vp], i),
         "pkv_selftest_wait_timeout": ([vp, vp, i, vp], i),
@@ -155,9 +156,18 @@ class Handle:
                                _stream(stream))
         self._check(st)
 
-    def kv_append(self, k, v, kv_layer, *, workspace, stream=None):
-        self._check(self.lib.pkv_kv_append(self.h, _dptr(k), _dptr(v), _dptr(kv_layer), _dptr(workspace),
-                                           _stream(stream)))
+    def kv_append(self, k, v, num_new_tokens, kv_layer, qo_indptr, kv_indptr, kv_indices, last_page_len, batch,
+                  stream=None):
+        """pkv_kv_append: k / v, the layer slice and the four index arrays are device
+        tensors (qo_indptr may be None: one new token per row)."""
+        self._check(self.lib.pkv_kv_append(self.h, _dptr(k), _dptr(v), int(num_new_tokens), _dptr(kv_layer),
+                                           _dptr(qo_indptr), _dptr(kv_indptr), _dptr(kv_indices),
+                                           _dptr(last_page_len), int(batch), _stream(stream)))
+
+    def kv_append_planned(self, k, v, kv_layer, *, workspace, stream=None):
+        """pkv_kv_append_planned: at the write locations of the last plan on `workspace`."""
+        self._check(self.lib.pkv_kv_append_planned(self.h, _dptr(k), _dptr(v), _dptr(kv_layer), _dptr(workspace),
+                                                   _stream(stream)))
 
     def _run(self, fn, q, kv_layer, out, lse, workspace, stream):
         self._check(fn(self.h, _dptr(q), _dptr(kv_layer), _dptr(out), _dptr(lse), _dptr(workspace), _stream(stream)))

@@ -623,6 +623,60 @@ __global__ void __launch_bounds__(256) append_kernel(const PlanHeader *hdr, cons
     cache[(row + page_size) * vec_per_token + c] = vv;
 }
 
+// Last-page append straight from the DEVICE index arrays (no plan): one thread per 16-byte
+// chunk of a new token's K and V rows.  Token t belongs to the row r with qo_indptr[r] <=
+// t < qo_indptr[r+1] (row t when qo_indptr is null: one token per row), sits at position
+// p = L_r - n_r + (t - qo_indptr[r]) of that row and lands in page
+// kv_indices[kv_indptr[r] + p / page_size] at slot p % page_size.  The arrays were not seen
+// by the host, so every index is checked before it is used: a token whose row arrays are
+// inconsistent (non-monotone offsets, a fill outside 1..page_size, a position outside the
+// row, a page id outside the cache) is not written, and nothing is read or written out of
+// bounds.
+__global__ void __launch_bounds__(256)
+    append_indexed_kernel(const uint4 *k, const uint4 *v, uint4 *cache, const int32_t *qo_indptr,
+                          const int32_t *kv_indptr, const int32_t *kv_indices, const int32_t *last_page_len, int batch,
+                          int num_tokens, int vec_per_token, int page_size, int page_shift, int num_cache_pages) {
+    griddep_wait();
+    griddep_launch();
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const int t = (int)(i / vec_per_token), c = (int)(i % vec_per_token);
+    if (t >= num_tokens) return;
+    int r, n, first;
+    if (qo_indptr) {
+        if (t >= __ldg(qo_indptr + batch)) return;
+        int lo = 0, hi = batch - 1;  // the last row whose offset is <= t
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (__ldg(qo_indptr + mid) <= t)
+                lo = mid;
+            else
+                hi = mid - 1;
+        }
+        r = lo;
+        first = __ldg(qo_indptr + r);
+        n = __ldg(qo_indptr + r + 1) - first;
+        if (first > t || t >= first + n) return;
+    } else {
+        if (t >= batch) return;
+        r = t;
+        first = t;
+        n = 1;
+    }
+    const int kb = __ldg(kv_indptr + r), ke = __ldg(kv_indptr + r + 1), nnz = __ldg(kv_indptr + batch);
+    const int fill = __ldg(last_page_len + r);
+    if (kb < 0 || ke <= kb || ke > nnz || fill < 1 || fill > page_size) return;
+    const long long L = (long long)(ke - kb - 1) * page_size + fill;
+    const long long p = L - n + (t - first);
+    if (p < 0 || p >= L) return;
+    const int page = __ldg(kv_indices + kb + (int)(p >> page_shift));
+    if (page < 0 || page >= num_cache_pages) return;
+    const size_t row = (size_t)page * 2 * page_size + (size_t)(p & (page_size - 1));
+    const uint4 kk = k[(size_t)t * vec_per_token + c];
+    const uint4 vv = v[(size_t)t * vec_per_token + c];
+    cache[row * vec_per_token + c] = kk;
+    cache[(row + page_size) * vec_per_token + c] = vv;
+}
+
 // Gather of a frozen prefix (DenseAttentionManager): one warp per position t copies
 // K and V of slot t % page_size of page pages[t / page_size] to row t of k_out / v_out.
 __global__ void __launch_bounds__(256) gather_kernel(const uint4 *cache, const int32_t *pages, int num_tokens,
@@ -779,6 +833,18 @@ cudaError_t launch_append(const Shape &s, const Plan &p, void *ws, const void *k
                       reinterpret_cast<const int32_t *>(w + p.lay.append_rows), vec, s.page_size);
 }
 
+cudaError_t launch_append_indexed(const Shape &s, const void *k, const void *v, int num_tokens, void *kv_layer,
+                                  const int32_t *qo_indptr, const int32_t *kv_indptr, const int32_t *kv_indices,
+                                  const int32_t *last_page_len, int batch, cudaStream_t st) {
+    if (num_tokens == 0 || batch == 0) return cudaSuccess;
+    const int vec = s.num_kv_heads * s.head_dim * 2 / 16;
+    const long long chunks = (long long)num_tokens * vec;
+    const int grid = (int)((chunks + 255) / 256);
+    return launch_pdl(dev::append_indexed_kernel, dim3(grid), dim3(256), 0, st, static_cast<const uint4 *>(k),
+                      static_cast<const uint4 *>(v), static_cast<uint4 *>(kv_layer), qo_indptr, kv_indptr, kv_indices,
+                      last_page_len, batch, num_tokens, vec, s.page_size, s.page_shift(), s.num_cache_pages);
+}
+
 }  // namespace pkv
 
 // ------------------------------------------------------------------------------------
@@ -796,23 +862,57 @@ static __device__ __align__(256) uint8_t g_decode_scratch[kStaticScratchBytes];
 
 size_t static_scratch_bytes() { return kStaticScratchBytes; }
 
-// Device address of g_decode_scratch on the current device.  The first call on a device
-// resolves it (with that device current) and caches it; later calls only read the cache.
+// Device address of g_decode_scratch in the current device's context.  The first call in
+// a context resolves it (with that device current) and caches it under the context's
+// unique id; a later call in another context -- another device, or the same device after
+// cudaDeviceReset made a new primary context -- resolves it again, so a cached address
+// never outlives the context it belongs to.
+namespace {
+using CtxGetCurrent = CUresult (*)(CUcontext *);
+using CtxGetId = CUresult (*)(CUcontext, unsigned long long *);
+template <typename F>
+cudaError_t driver_fn(const char *name, F *out) {
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion(name, &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorSymbolNotFound;
+    *out = reinterpret_cast<F>(fn);
+    return cudaSuccess;
+}
+}  // namespace
+
 cudaError_t static_scratch(void **ptr) {
+    static CtxGetCurrent ctx_get = nullptr;
+    static CtxGetId ctx_id = nullptr;
     static std::mutex mu;
-    static void *cached[128] = {};
+    static struct {
+        unsigned long long id;
+        void *addr;
+    } cached[128] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(mu);
-    if (!cached[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_decode_scratch);
-        if (e != cudaSuccess) return e;
-        cached[dev] = p;
+    if (!ctx_get && (e = driver_fn("cuCtxGetCurrent", &ctx_get)) != cudaSuccess) return e;
+    if (!ctx_id && (e = driver_fn("cuCtxGetId", &ctx_id)) != cudaSuccess) return e;
+    auto current_id = [&](unsigned long long *id) {
+        CUcontext ctx = nullptr;
+        return ctx_get(&ctx) == CUDA_SUCCESS && ctx && ctx_id(ctx, id) == CUDA_SUCCESS;
+    };
+    unsigned long long id = 0;
+    if (current_id(&id) && cached[dev].addr && cached[dev].id == id) {
+        *ptr = cached[dev].addr;
+        return cudaSuccess;
     }
-    *ptr = cached[dev];
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_decode_scratch);  // makes the primary context current if needed
+    if (e != cudaSuccess) return e;
+    if (!current_id(&id)) return cudaErrorDeviceUninitialized;
+    cached[dev].id = id;
+    cached[dev].addr = p;
+    *ptr = p;
     return cudaSuccess;
 }
 

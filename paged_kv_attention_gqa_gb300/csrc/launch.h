@@ -39,6 +39,10 @@ size_t prefill_smem_bytes(const Shape &s);
 
 cudaError_t launch_append(const Shape &s, const Plan &p, void *ws, const void *k, const void *v, void *kv_layer,
                           cudaStream_t st);
+// Append from device index arrays, no plan (pkv_kv_append); see append_indexed_kernel.
+cudaError_t launch_append_indexed(const Shape &s, const void *k, const void *v, int num_tokens, void *kv_layer,
+                                  const int32_t *qo_indptr, const int32_t *kv_indptr, const int32_t *kv_indices,
+                                  const int32_t *last_page_len, int batch, cudaStream_t st);
 // Decode pass (and the split-KV merge) of a DECODE or MIXED plan; `tm` boxes
 // (64 columns, Shape::dec_box_rows() rows, Shape::dec_heads() heads) of the layer slice.
 // `kv_layer` is the slice `tm` maps (read directly for pages below 8 slots).  With k_new /

@@ -294,9 +294,31 @@ static pkv_status pf_map(pkv_handle_t h, const void *kv) {
     return st;
 }
 
-extern "C" pkv_status pkv_kv_append(pkv_handle_t h, const void *k, const void *v, void *kv_layer, void *workspace,
-                                    pkv_stream_t stream) {
+extern "C" pkv_status pkv_kv_append(pkv_handle_t h, const void *k, const void *v, int num_new_tokens, void *kv_layer,
+                                    const int32_t *qo_indptr, const int32_t *kv_indptr, const int32_t *kv_indices,
+                                    const int32_t *last_page_len, int batch, pkv_stream_t stream) {
     NvtxCall nvtx_range(h, "pkv_kv_append");
+    if (!h) return fail(h, PKV_ERR_INVALID, "null handle");
+    if (num_new_tokens < 0 || batch < 0) return fail(h, PKV_ERR_INVALID, "num_new_tokens and batch must be >= 0");
+    if (batch > h->shape.max_batch) return fail(h, PKV_ERR_INVALID, "batch above max_batch");
+    if (!qo_indptr && num_new_tokens > batch)
+        return fail(h, PKV_ERR_INVALID, "without qo_indptr every row has one new token (num_new_tokens <= batch)");
+    if (num_new_tokens == 0 || batch == 0) return PKV_OK;
+    if (!k || !v || !kv_layer || !kv_indptr || !kv_indices || !last_page_len)
+        return fail(h, PKV_ERR_INVALID, "null k, v, kv_layer or index array");
+    if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(kv_layer)) % 16)
+        return fail(h, PKV_ERR_INVALID, "k, v and kv_layer must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(qo_indptr) | reinterpret_cast<uintptr_t>(kv_indptr) |
+         reinterpret_cast<uintptr_t>(kv_indices) | reinterpret_cast<uintptr_t>(last_page_len)) % 4)
+        return fail(h, PKV_ERR_INVALID, "index arrays must be 4-byte aligned");
+    cudaError_t e = pkv::launch_append_indexed(h->shape, k, v, num_new_tokens, kv_layer, qo_indptr, kv_indptr,
+                                               kv_indices, last_page_len, batch, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : cuda_fail(h, e, "append launch");
+}
+
+extern "C" pkv_status pkv_kv_append_planned(pkv_handle_t h, const void *k, const void *v, void *kv_layer,
+                                            void *workspace, pkv_stream_t stream) {
+    NvtxCall nvtx_range(h, "pkv_kv_append_planned");
     pkv_status st = check_planned(h, workspace, PKV_MODE_DECODE, PKV_MODE_PREFILL);
     if (st != PKV_OK && h && h->plan.mode == PKV_MODE_MIXED && h->planned_ws == workspace) st = PKV_OK;
     if (st != PKV_OK) return st;
@@ -502,6 +524,17 @@ extern "C" pkv_status pkv_run_decode_static(pkv_handle_t h, const void *q, const
     NvtxCall nvtx_range(h, "pkv_run_decode_static");
     if (!h) return fail(h, PKV_ERR_INVALID, "null handle");
     if (!(sm_scale >= 0.f) || std::isinf(sm_scale)) return fail(h, PKV_ERR_INVALID, "sm_scale must be finite and >= 0");
+    {
+        // The plan below is copied from host memory that is freed when this call returns;
+        // recorded into a graph, that copy would read freed memory when replayed.
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        cudaError_t ce = cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &cs);
+        if (ce != cudaSuccess) return cuda_fail(h, ce, "stream capture status");
+        if (cs != cudaStreamCaptureStatusNone)
+            return fail(h, PKV_ERR_INVALID,
+                        "pkv_run_decode_static copies its plan from host memory it frees on return, so it does "
+                        "not run on a stream that is capturing");
+    }
     std::string err;
     Plan plan;
     int rc = pkv::make_plan(h->shape, PKV_MODE_DECODE, nullptr, kv_indptr, kv_indices, last_page_len, batch, 1,

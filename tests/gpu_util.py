@@ -46,7 +46,7 @@ def gpu_step(pb, x, mode, *, layer=0, window_left=-1, causal=True, sm_scale=0.0,
         h.run_decode_append(q, x["k_new"], x["v_new"], kv, out, lse, workspace=ws)
     else:
         if append and x.get("k_new") is not None:
-            h.kv_append(x["k_new"], x["v_new"], kv, workspace=ws)
+            h.kv_append_planned(x["k_new"], x["v_new"], kv, workspace=ws)
         getattr(h, "run_" + mode)(q, kv, out, lse, workspace=ws)
     torch.cuda.synchronize()
     assert h.check_device_error(ws) == 0
@@ -101,3 +101,44 @@ def compact_rows(pb, kv_bits, rows, extra_pages=()):
                         pb.kv_lens[rows], pb.qo_lens[rows], [np.array([remap[int(p)] for p in pb.page_table[r]])
                                                              for r in rows], len(pages))
     return sub, kv_bits[np.asarray(pages, np.int64)], remap
+
+
+def causal_subrows(pb, max_tokens=256):
+    """The same causal attention as smaller independent rows: each row's new tokens are cut
+    into runs of at most `max_tokens`, and a run ending at position e (exclusive) becomes a
+    row of length e over the parent's first ceil(e / P) pages.  A causal query at position
+    p sees keys 0..p only, so the run's queries see exactly the keys they see in the parent
+    row; the runs keep the parent's token order, so the result lines up with q / out of
+    the parent batch.  Lets the oracle spread one long row over several threads."""
+    P = pb.page_size
+    qo, kvp, kvi, _ = pb.index_arrays()
+    n_qo, n_kvp, n_kvi, n_lpl = [0], [0], [], []
+    for r in range(pb.batch):
+        L, n = int(pb.kv_lens[r]), int(pb.qo_lens[r])
+        c = L - n
+        starts = list(range(0, n, max_tokens)) if n else [0]
+        for a in starts:
+            b = min(n, a + max_tokens)
+            e = c + b  # length of the sub-row: up to its last query
+            if e == 0:
+                n_qo.append(n_qo[-1])
+                n_kvp.append(n_kvp[-1])
+                n_lpl.append(0)
+                continue
+            pages = -(-e // P)
+            n_kvi.extend(int(p) for p in kvi[kvp[r]: kvp[r] + pages])
+            n_kvp.append(len(n_kvi))
+            n_qo.append(n_qo[-1] + (b - a))
+            n_lpl.append((e - 1) % P + 1)
+    i32 = lambda a: np.asarray(a, np.int32)
+    assert n_qo[-1] == pb.num_tokens
+    return i32(n_qo), i32(n_kvp), i32(n_kvi), i32(n_lpl)
+
+
+def oracle_attn_causal_split(pb, q_bits, kv_bits, *, window_left=-1, threads=16, max_tokens=256):
+    """oracle.attention over causal_subrows(pb): identical per-token definition, rows
+    small enough to balance over the threads."""
+    qo, kvp, kvi, lpl = causal_subrows(pb, max_tokens)
+    return oracle.attention(q_bits, kv_bits, qo, kvp, kvi, lpl, num_qo_heads=pb.num_qo_heads,
+                            num_kv_heads=pb.num_kv_heads, head_dim=pb.head_dim, page_size=pb.page_size,
+                            causal=True, window_left=window_left, threads=threads)

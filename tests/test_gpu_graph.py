@@ -84,12 +84,12 @@ def test_captured_step_replays_after_replanning(mode):
     # one uncaptured call of each kind, then the capture
     load(steps[0], 0)
     plan(steps[0])
-    h.kv_append(k, v, kv, workspace=ws)
+    h.kv_append_planned(k, v, kv, workspace=ws)
     run(q, kv, out, lse, workspace=ws)
     torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
-        h.kv_append(k, v, kv, workspace=ws)
+        h.kv_append_planned(k, v, kv, workspace=ws)
         run(q, kv, out, lse, workspace=ws)
     torch.cuda.synchronize()
 

@@ -198,36 +198,54 @@ def test_mixed_poisoned_sink_rows_do_not_leak():
 # ------------------------------------------------------------------ full-size workloads (launch configuration of bench.py)
 
 def test_batch_decode_full_size():
+    """The bench's step: one plan, then one fused append + decode launch per layer over the
+    32-layer cache.  Layers 0 and 31: the whole appended slice bit-exact and every row
+    against the oracle.  Every other layer: a seeded 8-row sample against the oracle and
+    its appended slots bit-exact."""
     pb = wl.config_batch_decode()
     x = wl.make_inputs(pb, device="cuda", seed=0, unused="randn")
     h = G.make_handle(pb)
     ws = torch.empty(h.workspace_size(0), dtype=torch.uint8, device="cuda")
     h.plan(0, None, pb.kv_indptr, pb.kv_indices, pb.last_page_len, workspace=ws)
-    check_layers = {0: None, 31: None, 13: [3, 77, 127]}
-    befores = {l: wl.bf16_bits(x["kv_cache"][l]) for l in check_layers}
+    rng = np.random.default_rng(2024)
+    check_layers = {l: None if l in (0, pb.num_layers - 1) else sorted(rng.choice(pb.batch, 8, replace=False))
+                    for l in range(pb.num_layers)}
+    befores = {l: wl.bf16_bits(x["kv_cache"][l]) for l, rows in check_layers.items() if rows is None}
     outs = {}
     for l in range(pb.num_layers):  # as bench.py runs the step: one fused launch per layer
         kv = x["kv_cache"][l]
         out = torch.empty_like(x["q"])
         lse = torch.empty(pb.batch, pb.num_qo_heads, dtype=torch.float32, device="cuda")
         h.run_decode_append(x["q"], x["k_new"], x["v_new"], kv, out, lse, workspace=ws)
-        if l in check_layers:
-            outs[l] = (out, lse)
+        outs[l] = (out, lse)
     torch.cuda.synchronize()
     assert h.check_device_error(ws) == 0
+    k_bits, v_bits = wl.bf16_bits(x["k_new"]), wl.bf16_bits(x["v_new"])
+    P = pb.page_size
     for l, rows in check_layers.items():
-        after = G.oracle_append(pb, befores[l], x)
-        assert np.array_equal(wl.bf16_bits(x["kv_cache"][l]), after), l
+        after = wl.bf16_bits(x["kv_cache"][l])
+        if rows is None:
+            assert np.array_equal(after, G.oracle_append(pb, befores[l], x)), l
+        else:
+            for r in rows:  # the row's new token at (last page, last slot)
+                page, slot = int(pb.page_table[r][(int(pb.kv_lens[r]) - 1) // P]), (int(pb.kv_lens[r]) - 1) % P
+                assert np.array_equal(after[page, 0, slot], k_bits[r]), (l, r)
+                assert np.array_equal(after[page, 1, slot], v_bits[r]), (l, r)
         ref_o, ref_l = G.oracle_attn(pb, wl.bf16_bits(x["q"]), after, rows=rows, threads=16)
         G.compare(*outs[l], ref_o, ref_l, tokens=None if rows is None else G.token_mask(pb, rows), what=f"layer {l}")
 
 
 def test_ragged_prefill_full_size():
+    """Every token of every row of the timed prefill workload against the oracle (its rows
+    cut into causal runs so the oracle spreads them over 16 threads)."""
     pb = wl.config_prefill()
-    # rows the oracle finishes in seconds: row 0 (prefix 0) and the cheapest others
-    cost = pb.qo_lens * (pb.kv_lens - pb.qo_lens + pb.qo_lens / 2)
-    rows = sorted(set([0] + list(np.argsort(cost)[:3])))
-    _check_step(pb, "prefill", unused="randn", rows=rows)
+    x = wl.make_inputs(pb, device="cuda", seed=0, unused="randn", layers=1)
+    before = wl.bf16_bits(x["kv_cache"][0])
+    out, lse, h, ws = G.gpu_step(pb, x, "prefill")
+    after = G.oracle_append(pb, before, x)
+    assert np.array_equal(wl.bf16_bits(x["kv_cache"][0]), after), "appended cache differs from the oracle's"
+    ref_o, ref_l = G.oracle_attn_causal_split(pb, wl.bf16_bits(x["q"]), after)
+    G.compare(out, lse, ref_o, ref_l, what="ragged prefill, all 16 rows")
 
 
 def test_mixed_full_size():

@@ -1,4 +1,4 @@
-"""Shapes beyond page_size 16: page sizes 1 .. 64, head_dim 256, group sizes that are not
+"""Shapes beyond page_size 16: page sizes 1 .. 64 and 128 .. 1024, head_dim 256, group sizes that are not
 powers of two, and more than 8 kv heads (decode then splits the kv heads over CTA groups),
 each through the C ABI against the oracle on the same seeded inputs.
 
@@ -113,6 +113,51 @@ def test_mixed_page_sizes(P):
                    reserve_sink=True)
     pb.max_prefill_rows = int((np.asarray(n) >= 2).sum()) + 1
     _check_step(pb, "mixed", seed=5)
+
+
+# ------------------------------------------------------------------ pages of 128 to 1024 slots
+
+LARGE_PAGES = [128, 256, 1024]
+
+
+@pytest.mark.parametrize("P", LARGE_PAGES)
+@pytest.mark.parametrize("Hq,Hkv,D", [(32, 8, 128), (8, 1, 64), (16, 4, 256)])
+@pytest.mark.parametrize("fused", [False, True])
+def test_decode_large_pages(P, Hq, Hkv, D, fused):
+    lens = _decode_lens(P)
+    pb = wl.custom(160 + P, lens, [1] * len(lens), num_qo_heads=Hq, num_kv_heads=Hkv, head_dim=D, page_size=P,
+                   pool_factor=1.3)
+    _check_step(pb, "decode", seed=P + 11, fused=fused)
+
+
+@pytest.mark.parametrize("P", LARGE_PAGES)
+@pytest.mark.parametrize("sm_count,window", [(1, -1), (3, -1), (40, -1), (40, 100), (0, 0)])
+def test_decode_large_pages_splits_and_windows(P, sm_count, window):
+    """Pieces cut at the boundaries of long pages (few pages per row) through both merges,
+    and windows that start inside a page."""
+    lens = [3 * P + 5, 5, P, 1, 2 * P - 3, 7000]
+    pb = wl.custom(170 + P, lens, [1] * len(lens), num_qo_heads=32, num_kv_heads=8, head_dim=128, page_size=P)
+    _check_step(pb, "decode", sm_count=sm_count, window_left=window, seed=P + 12, fused=sm_count == 3)
+
+
+@pytest.mark.parametrize("P", LARGE_PAGES)
+@pytest.mark.parametrize("Hq,Hkv,D", [(32, 8, 128), (8, 2, 64), (8, 4, 256)])
+@pytest.mark.parametrize("causal,window", [(True, -1), (False, -1), (True, 200)])
+def test_prefill_large_pages(P, Hq, Hkv, D, causal, window):
+    n = [1, 7, 33, 300, 64, 2]
+    c = [0, 40, 0, P + 9, 2 * P, 1]
+    pb = wl.custom(180 + P, np.add(n, c), n, num_qo_heads=Hq, num_kv_heads=Hkv, head_dim=D, page_size=P)
+    _check_step(pb, "prefill", causal=causal, window_left=window, seed=P + 13)
+
+
+@pytest.mark.parametrize("P", LARGE_PAGES)
+def test_mixed_large_pages(P):
+    n = [1, 1, 40, 1, 3, 1, 0, 1, 100]
+    c = [20, 3 * P, 10, 1, 0, P, 5, 700, 33]
+    pb = wl.custom(190 + P, np.add(n, c), n, num_qo_heads=32, num_kv_heads=8, head_dim=128, page_size=P,
+                   reserve_sink=True)
+    pb.max_prefill_rows = int((np.asarray(n) >= 2).sum()) + 1
+    _check_step(pb, "mixed", seed=P + 14)
 
 
 # ------------------------------------------------------------------ head_dim 256
@@ -253,12 +298,12 @@ def test_graph_mode_shapes(P, D, Hq, Hkv):
     out = torch.empty_like(q)
     lse = torch.empty(q.shape[:2], dtype=torch.float32, device="cuda")
     h.plan(B.MODE_DECODE, None, pbs[0].kv_indptr, pbs[0].kv_indices, pbs[0].last_page_len, workspace=ws)
-    h.kv_append(k_new, v_new, kv, workspace=ws)
+    h.kv_append_planned(k_new, v_new, kv, workspace=ws)
     h.run_decode(q, kv, out, lse, workspace=ws)
     torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
-        h.kv_append(k_new, v_new, kv, workspace=ws)
+        h.kv_append_planned(k_new, v_new, kv, workspace=ws)
         h.run_decode(q, kv, out, lse, workspace=ws)
     torch.cuda.synchronize()
     for i, pb in enumerate(pbs):
@@ -322,12 +367,12 @@ def test_graph_mode_prefill_page_sizes(P):
 
     load(pbs[0], 20)
     plan(pbs[0])
-    h.kv_append(k, v, kv, workspace=ws)
+    h.kv_append_planned(k, v, kv, workspace=ws)
     h.run_prefill(q, kv, out, lse, workspace=ws)
     torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
-        h.kv_append(k, v, kv, workspace=ws)
+        h.kv_append_planned(k, v, kv, workspace=ws)
         h.run_prefill(q, kv, out, lse, workspace=ws)
     torch.cuda.synchronize()
     for i, pb in enumerate(pbs[::-1]):
