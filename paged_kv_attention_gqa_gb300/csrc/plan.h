@@ -161,6 +161,13 @@ struct Shape {
     // gathered with 16-byte cp.async copies instead (a box would not fill a swizzle atom).
     bool pf_gather() const { return page_size < 8; }
     int pf_box_rows() const { return page_size < 16 ? page_size : 16; }
+    // Prefill work tiles of two query tiles (2 x 128 rows sharing every 128-key K/V tile,
+    // one CTA per SM): head_dim 64 and 128 with K / V read by TMA (dense plans always are);
+    // head_dim 256 and the cp.async gather of small pages keep one query tile per CTA.
+    bool pf_pair(bool dense) const { return head_dim <= 128 && (dense || !pf_gather()); }
+    int pf_tile_tokens(bool dense) const {
+        return (kPrefillRowsPerTile / group()) * (pf_pair(dense) ? 2 : 1);
+    }
 };
 
 // Worst-case counts at a handle's maxima for one plan mode: the launch grids and the

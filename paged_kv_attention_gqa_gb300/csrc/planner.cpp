@@ -301,9 +301,9 @@ struct PrefillRow {
 };
 
 static void prefill_tiles_rows(const Shape &s, const std::vector<PrefillRow> &rows, int causal, int window_left,
-                               std::vector<PrefillTile> &out) {
-    const int g = s.group();
-    const int BQ = kPrefillRowsPerTile / g;
+                               std::vector<PrefillTile> &out, bool dense = false) {
+    // tokens per work tile: one query tile of 128 / g tokens, or two on the paired kernel
+    const int BQ = s.pf_tile_tokens(dense);
     for (const PrefillRow &pr : rows) {
         const int n = pr.n, L = pr.L;
         if (n <= 0) continue;
@@ -357,7 +357,7 @@ static void prefill_tiles(const Shape &s, const std::vector<int> &rows, const in
 
 // Time model of one GB300 used to share the SMs between the two passes of a mixed step:
 // streaming K/V at ~6.4 TB/s, prefill tiles at ~0.9 PFLOP/s (both measured on this
-// library's own kernels).
+// library's own kernels; the flops count every query row of a tile).
 constexpr double kDecodeBytesPerUs = 6.4e6;
 constexpr double kPrefillFlopsPerUs = 0.9e9;
 
@@ -371,7 +371,8 @@ static int mixed_decode_ctas(const Shape &s, int rows, const int32_t *kvp, const
         const int lo = window_left >= 0 ? std::max(0, L - 1 - window_left) : 0;
         bytes += (double)(L - lo) * s.num_kv_heads * s.head_dim * 4.0;
     }
-    for (const PrefillTile &t : ptiles) flops += 4.0 * kPrefillRowsPerTile * s.head_dim * (t.key_end - t.key_begin);
+    const double tile_rows = (double)kPrefillRowsPerTile * (s.pf_pair(false) ? 2 : 1);
+    for (const PrefillTile &t : ptiles) flops += 4.0 * tile_rows * s.head_dim * (t.key_end - t.key_begin);
     const double t_dec = bytes / kDecodeBytesPerUs, t_pf = flops / kPrefillFlopsPerUs;
     const int pf_sms = (int)(C * t_pf / (t_dec + t_pf) + 0.5);
     return std::max(C / 4, std::min(C, C - pf_sms));
@@ -626,7 +627,7 @@ int make_dense_plan(const Shape &s, const int32_t *cu_q, const int32_t *cu_k, in
     plan.num_tokens = cu_q[batch];
     plan.num_keys = cu_k[batch];
     std::vector<PrefillTile> ptiles;
-    prefill_tiles_rows(s, rows, causal, window_left, ptiles);
+    prefill_tiles_rows(s, rows, causal, window_left, ptiles, true);
     std::vector<int32_t> none, cta;
     finish_plan(s, plan, plan.num_tokens, window_left, none, none, none, {}, cta, {}, ptiles, 0);
     return PKV_OK;

@@ -41,6 +41,8 @@ cudaError_t launch_prefill(const Shape &s, const Plan &p, const CUtensorMap &tm_
     const size_t smem = prefill_smem_bytes(s);
     cudaError_t e = cudaErrorInvalidValue;
     const int g = s.group();
+    if (s.pf_pair(p.mode == PKV_MODE_DENSE))  // two query tiles per CTA (prefill_pair.cuh)
+        return launch_prefill_pair(s.head_dim, g, tm_kv, tm_v, tm_q, a, grid, st);
     if (a.gather && p.mode != PKV_MODE_DENSE)  // dense plans always read K / V by TMA
         return launch_prefill_gather(s.head_dim, g, tm_kv, tm_v, tm_q, a, grid, smem, st);
 #define PKV_PF(DD, GG) \

@@ -490,6 +490,9 @@ __global__ void __launch_bounds__(GATHER ? kPfGatherThreads : kPfThreads, D > 12
 
 }  // namespace dev
 
+// Two query tiles per CTA, head_dim 64 / 128 read by TMA: prefill_pair.cu.
+cudaError_t launch_prefill_pair(int head_dim, int group, const CUtensorMap &tkv, const CUtensorMap &tv,
+                                const CUtensorMap &tq, const dev::PrefillArgs &a, int grid, cudaStream_t st);
 // Instances with GATHER = true live in prefill_gather.cu (compiled in parallel).
 cudaError_t launch_prefill_gather(int head_dim, int group, const CUtensorMap &tkv, const CUtensorMap &tv,
                                   const CUtensorMap &tq, const dev::PrefillArgs &a, int grid, size_t smem,
