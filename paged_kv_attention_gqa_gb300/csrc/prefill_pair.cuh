@@ -230,8 +230,6 @@ __global__ void __launch_bounds__(kPpThreads, 1)
         const int tail_end = (t.length + P - 1) & ~(P - 1);
         bool ok = mbar_wait(&q_full[x], 0, err, kErrWaitFull);
         uint32_t i = 0;  // ring slot sequence, as the producer counts it
-        // K_0 here; K_{j+1} at the end of iteration j, while PV_X(j) still runs, so that the
-        // wait for PV_X(j) is the only one between it and S_X(j+1)
         if (ok && nt > 0) ok = mbar_wait(&kv_full[0], 0, err, kErrWaitFull);
         for (int j = 0; j < nt && ok; ++j, i += 2) {
             const int sk = i % NS, sv = (i + 1) % NS;
@@ -274,7 +272,10 @@ __global__ void __launch_bounds__(kPpThreads, 1)
                     if (!ok) break;
                 }
             }
-            ok = mbar_wait(&p_full[x], j & 1, err, kErrWaitFull);
+            // K_{j+1} is awaited here, while the softmax still runs, so that after PV_X(j) only
+            // its own completion stands between it and S_X(j+1)
+            if (j + 1 < nt) ok = mbar_wait(&kv_full[(i + 2) % NS], ((i + 2) / NS) & 1, err, kErrWaitFull);
+            if (ok) ok = mbar_wait(&p_full[x], j & 1, err, kErrWaitFull);
             if (!ok) break;
             tc_fence_after();
             {
@@ -286,7 +287,6 @@ __global__ void __launch_bounds__(kPpThreads, 1)
                 mma_commit_elect(&kv_empty[sv]);  // V_j's stage frees once both tiles' PV MMAs completed
                 if (j == nt - 1) mma_commit_elect(&o_final[x]);
             }
-            if (j + 1 < nt) ok = mbar_wait(&kv_full[(i + 2) % NS], ((i + 2) / NS) & 1, err, kErrWaitFull);
         }
         if (nt == 0 && lane == 0) mma_commit(&o_final[x]);  // no MMA: arrives at once
     }
@@ -342,21 +342,39 @@ __global__ void __launch_bounds__(kPpThreads, 1)
                         sv[c] = (k >= lo && k <= hi && k < t.length) ? sv[c] : -INFINITY;
                     }
                 }
-                float mx;
-                {
-                    float a0 = sv[0], a1 = sv[1], a2 = sv[2], a3 = sv[3];
+                // p = 2^(s * sl - mref), two columns per packed FMA; sums in four packed chains;
+                // P goes back over the S columns as packed bf16 (64 columns), in two halves
+                uint64_t acc[4];
+                auto exp_pass = [&](float mref) {
+                    const uint64_t sl2 = f2_make(sl, sl), nm2 = f2_make(-mref, -mref);
+                    acc[0] = acc[1] = acc[2] = acc[3] = 0;
 #pragma unroll
-                    for (int c = 4; c < kPpKeys - 4; c += 8) {
-                        a0 = max3f(a0, sv[c], sv[c + 1]);
-                        a1 = max3f(a1, sv[c + 2], sv[c + 3]);
-                        a2 = max3f(a2, sv[c + 4], sv[c + 5]);
-                        a3 = max3f(a3, sv[c + 6], sv[c + 7]);
+                    for (int hlf = 0; hlf < 2; ++hlf) {
+                        uint32_t pk[32];
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) {
+                            const int e = hlf * 64 + 2 * c;
+                            float x0, x1;
+                            f2_split(ffma2(f2_make(sv[e], sv[e + 1]), sl2, nm2), x0, x1);
+                            const float p0 = ex2_ftz(x0), p1 = ex2_ftz(x1);
+                            acc[c & 3] = fadd2(acc[c & 3], f2_make(p0, p1));
+                            pk[c] = pack_bf16(p0, p1);
+                        }
+                        tmem_st32(Sx + hlf * 32, pk);
                     }
-                    a0 = max3f(a0, sv[kPpKeys - 4], sv[kPpKeys - 3]);
-                    a1 = max3f(a1, sv[kPpKeys - 2], sv[kPpKeys - 1]);
-                    mx = max3f(fmaxf(a0, a1), a2, a3);
-                }
-                const float m_tile = mx * sl;  // -inf when the whole tile is masked for this row
+                };
+                // the tile's row maximum: eight independent chains of 3-input max
+                auto tile_max = [&]() {
+                    float m8[8];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) m8[c] = fmaxf(sv[2 * c], sv[2 * c + 1]);
+#pragma unroll
+                    for (int c = 16; c < kPpKeys; c += 16)
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) m8[q] = max3f(m8[q], sv[c + 2 * q], sv[c + 2 * q + 1]);
+                    return max3f(max3f(m8[0], m8[1], m8[2]), max3f(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7])) * sl;
+                };
+                const float m_tile = tile_max();  // -inf when the whole tile is masked for this row
                 // move the running max only when it grows by more than the threshold
                 const bool grow = m_tile > m_run + kRescaleThreshold;
                 const bool warp_grow = __any_sync(0xffffffffu, grow) && j > 0;
@@ -368,25 +386,7 @@ __global__ void __launch_bounds__(kPpThreads, 1)
                         m_run = m_new;
                     }
                 }
-                const float mref = m_run == -INFINITY ? 0.f : m_run;
-                // p = 2^(s * sl - mref), two columns per packed FMA; sums in four packed chains;
-                // P goes back over the S columns as packed bf16 (64 columns), in two halves
-                const uint64_t sl2 = f2_make(sl, sl), nm2 = f2_make(-mref, -mref);
-                uint64_t acc[4] = {0, 0, 0, 0};
-#pragma unroll
-                for (int hlf = 0; hlf < 2; ++hlf) {
-                    uint32_t pk[32];
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        const int e = hlf * 64 + 2 * c;
-                        float x0, x1;
-                        f2_split(ffma2(f2_make(sv[e], sv[e + 1]), sl2, nm2), x0, x1);
-                        const float p0 = ex2_ftz(x0), p1 = ex2_ftz(x1);
-                        acc[c & 3] = fadd2(acc[c & 3], f2_make(p0, p1));
-                        pk[c] = pack_bf16(p0, p1);
-                    }
-                    tmem_st32(Sx + hlf * 32, pk);
-                }
+                exp_pass(m_run == -INFINITY ? 0.f : m_run);
                 float u0, u1;
                 f2_split(fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3])), u0, u1);
                 l_run = l_run * alpha + (u0 + u1);
