@@ -440,8 +440,8 @@ def run_step_primary(args, rank, world):
         achieved = fl / (kms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": round(achieved / peaks["bf16_tflops"], 4),
-                "traffic": kernel_traffic("prefill_kernel.cuh", "prefill_ragged16_tcgen05.md"),
-                "kernel": "prefill_tc_kernel",
+                "traffic": kernel_traffic("prefill_pair.cuh", "prefill_ragged16_pair.md"),
+                "kernel": "prefill_pair_kernel",
                 "launch_ms": round(kms, 5), "peak_source": peaks["source"]}
         launches = 2
     else:
@@ -521,7 +521,7 @@ def secondary(B, dev, peaks, seed):
                       "append_ms": round(app_ms, 4),
                       # DRAM bytes of one launch from the committed ncu capture (None once the
                       # kernel source differs from the captured one)
-                      "traffic": kernel_traffic("prefill_kernel.cuh", "prefill_ragged16_tcgen05.md")}
+                      "traffic": kernel_traffic("prefill_pair.cuh", "prefill_ragged16_pair.md")}
     del x, kv
     # mixed step
     pb = wl.config_mixed(seed=seed)
