@@ -545,26 +545,54 @@ __global__ void __launch_bounds__((D > 128 ? 4 + (SMALL ? 2 : 1) : 8 + (SMALL ? 
 // the row is in flight at once, and the slots are added through shared memory.
 constexpr int kMergeThreads = 256;
 
+// Pieces of a row whose weights warp 0 keeps in shared memory and whose partial columns the
+// threads request before those weights are known; rows with more pieces take a second loop.
+constexpr int kMergeFastPieces = 32;
+
+template <int D>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const PlanHeader *hdr, const MergeRow *rows,
                                                               const float *part_o, const float *part_lse,
-                                                              __nv_bfloat16 *out, float *lse, int Hq, int D) {
+                                                              __nv_bfloat16 *out, float *lse, int Hq) {
+    constexpr int PER = D / 4;                      // threads per piece row (4 columns each)
+    constexpr int SLOTS = kMergeThreads / PER;      // pieces the CTA reads side by side
+    constexpr int NPER = kMergeFastPieces / SLOTS;  // pieces per thread requested up front
     __shared__ float4 s_acc[kMergeThreads];
+    __shared__ float s_w[kMergeFastPieces];
     __shared__ float s_red[2];
+    // the plan's own values (copied before the decode launch) are read before waiting for the
+    // decode kernel; the partials it writes only after
+    const bool active = !hdr->fused_merge && (int)blockIdx.x < hdr->num_merge;
+    MergeRow mr{};
+    if (active) mr = rows[blockIdx.x];
     griddep_wait();
     griddep_launch();
-    if (hdr->fused_merge || (int)blockIdx.x >= hdr->num_merge) return;
-    const MergeRow mr = rows[blockIdx.x];
-    if (mr.out_token < 0) return;
+    if (!active || mr.out_token < 0) return;
     const int h = blockIdx.y;
     const int count = mr.count;
     const float *lse_of = part_lse + (size_t)mr.first * Hq + h;  // piece j at lse_of[j * Hq]
+    const int slot = threadIdx.x / PER, c = (threadIdx.x % PER) * 4;
+    auto piece_o = [&](int j) {
+        return __ldcg(reinterpret_cast<const float4 *>(part_o + ((size_t)(mr.first + j) * Hq + h) * D + c));
+    };
+    // this thread's first pieces' partial columns: requested before the weights are known
+    float4 v[NPER];
+#pragma unroll
+    for (int k = 0; k < NPER; ++k) {
+        const int j = slot + k * SLOTS;
+        v[k] = j < count ? piece_o(j) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    // warp 0: M = max_j lse_j, w_j = exp(lse_j - M) (the first pieces' into shared memory), sum w_j
     if (threadIdx.x < 32) {
         float M = -INFINITY;
         for (int j = threadIdx.x; j < count; j += 32) M = fmaxf(M, __ldcg(lse_of + (size_t)j * Hq));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
         float sum = 0.f;
-        for (int j = threadIdx.x; j < count; j += 32) sum += __expf(__ldcg(lse_of + (size_t)j * Hq) - M);
+        for (int j = threadIdx.x; j < count; j += 32) {
+            const float w = __expf(__ldcg(lse_of + (size_t)j * Hq) - M);
+            if (j < kMergeFastPieces) s_w[j] = w;
+            sum += w;
+        }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
         if (threadIdx.x == 0) {
@@ -574,30 +602,22 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const PlanHeader *
     }
     __syncthreads();
     const float M = s_red[0];
-    // weighted partial sums: slot = threadIdx / (D/4), 4 columns each
-    const int per_piece = D / 4;
-    const int slots = kMergeThreads / per_piece;
-    const int slot = threadIdx.x / per_piece, c = (threadIdx.x % per_piece) * 4;
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int j = slot; j < count; j += slots) {
-        const float w = __expf(__ldcg(lse_of + (size_t)j * Hq) - M);
-        const float4 v = __ldcg(reinterpret_cast<const float4 *>(part_o + ((size_t)(mr.first + j) * Hq + h) * D + c));
-        o.x += w * v.x;
-        o.y += w * v.y;
-        o.z += w * v.z;
-        o.w += w * v.w;
-    }
+    auto add = [&](float w, const float4 &x) {
+        o.x += w * x.x;
+        o.y += w * x.y;
+        o.z += w * x.z;
+        o.w += w * x.w;
+    };
+#pragma unroll
+    for (int k = 0; k < NPER; ++k)
+        if (slot + k * SLOTS < count) add(s_w[slot + k * SLOTS], v[k]);
+    for (int j = slot + NPER * SLOTS; j < count; j += SLOTS)  // rows of many pieces
+        add(__expf(__ldcg(lse_of + (size_t)j * Hq) - M), piece_o(j));
     s_acc[threadIdx.x] = o;
     __syncthreads();
     if (slot == 0) {
-        for (int k = 1; k < slots; ++k) {
-            const float4 v = s_acc[k * per_piece + threadIdx.x];
-            o.x += v.x;
-            o.y += v.y;
-            o.z += v.z;
-            o.w += v.w;
-        }
+        for (int k = 1; k < SLOTS; ++k) add(1.f, s_acc[k * PER + threadIdx.x]);
         const float inv = 1.f / s_red[1];
         __nv_bfloat16 *dst = out + ((size_t)mr.out_token * Hq + h) * D + c;
         *reinterpret_cast<uint2 *>(dst) = make_uint2(pack_bf16(o.x * inv, o.y * inv), pack_bf16(o.z * inv, o.w * inv));
@@ -811,10 +831,10 @@ cudaError_t launch_decode(const Shape &s, const Plan &p, const CUtensorMap &tm, 
     const int merges = s.graph_static ? sc.num_merge : (p.fused_merge ? 0 : p.num_merge);
     if (merges) {
         const dim3 mgrid(merges, s.num_qo_heads);
-        e = launch_pdl(dev::merge_kernel, mgrid, dim3(dev::kMergeThreads), 0, st,
-                       static_cast<const PlanHeader *>(a.hdr), reinterpret_cast<const MergeRow *>(w + p.lay.merge_rows),
-                       static_cast<const float *>(a.part_o), static_cast<const float *>(a.part_lse), a.out, lse,
-                       s.num_qo_heads, s.head_dim);
+        auto mk = s.head_dim == 64 ? dev::merge_kernel<64> : s.head_dim == 128 ? dev::merge_kernel<128> : dev::merge_kernel<256>;
+        e = launch_pdl(mk, mgrid, dim3(dev::kMergeThreads), 0, st, static_cast<const PlanHeader *>(a.hdr),
+                       reinterpret_cast<const MergeRow *>(w + p.lay.merge_rows), static_cast<const float *>(a.part_o),
+                       static_cast<const float *>(a.part_lse), a.out, lse, s.num_qo_heads);
     }
     return e;
 }
