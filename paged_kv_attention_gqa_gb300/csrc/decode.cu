@@ -11,9 +11,8 @@
 //    batch's visible pages (balanced to +-1 page); a row cut by a CTA boundary writes an
 //    fp32 partial (o normalised, lse) into the workspace, merged afterwards.
 //  * The slots of one page are contiguous for ALL kv heads (K: page_size x Hkv x D, then
-//    V), so a CTA streams 16-key chunks of its heads: the producer warp issues TMA boxes
-//    (64-column halves, 128-byte swizzle; one lane per box, the next chunk's page looked up
-//    while the warp waits for a free stage) into a ring of stages, completion on an
+//    V), so a CTA streams 16-key chunks of its heads: one producer thread issues TMA
+//    boxes (64-column halves, 128-byte swizzle) into a ring of stages, completion on an
 //    mbarrier; consumers release a stage through a second mbarrier.  A chunk is one box
 //    of K and one of V (page size >= 16) or two of each (8); pages below 8 slots are
 //    copied by the whole producer warp with 16-byte cp.async into the same layout.
@@ -243,84 +242,74 @@ __global__ void __launch_bounds__((D > 128 ? 4 + (SMALL ? 2 : 1) : 8 + (SMALL ? 
     }
     if (warp >= Hc) {
         if (warp > Hc) return;
-        // ---------------- producer warp ----------------
-        const int nkv = 2;
-        const uint32_t box_bytes = (uint32_t)a.box_rows * Hc * 128;
-        uint32_t it = 0;
-        if (!SMALL) {
-            // One box of K and one of V per chunk, each in HALVES 64-column halves: lane b
-            // issues box b (one thread's tensor copies issue a few hundred cycles apart); lane
-            // 0 waits for the slot and announces the bytes.  The warp looks up the next
-            // chunk's slot row while it waits for this chunk's slot.
-            constexpr int BPC = 2 * HALVES;
-            const int kv = lane / HALVES, half = lane % HALVES;
-            bool ok = true;
-            for (int ti = t_begin; ti < t_end && ok; ++ti) {
-                const DecodeTile t = a.tiles[ti];
-                const ChunkRange cr = chunk_range(t, P);
-                auto chunk_row = [&](int k) {
-                    const int pos0 = cr.base + k * kDecodeKeysPerStage;
-                    return a.pages[t.kv_base + (pos0 >> a.page_shift)] * 2 * P + (pos0 & (P - 1));
-                };
-                int row = cr.k0 < cr.nk ? chunk_row(cr.k0) : 0;
-                for (int k = cr.k0; k < cr.nk; ++k, ++it) {
-                    const int row_next = k + 1 < cr.nk ? chunk_row(k + 1) : 0;
-                    const int s = it % a.stages;
-                    const uint32_t use = it / a.stages;
-                    bool w = true;
-                    if (lane == 0) {
-                        w = use == 0 || mbar_wait(&empty[s], (use - 1) & 1, err, kErrWaitEmpty);
-                        if (w) mbar_arrive_expect_tx(&full[s], (uint32_t)BPC * box_bytes);
-                    }
-                    if (!__shfl_sync(0xffffffffu, w ? 1 : 0, 0)) {
-                        ok = false;
-                        break;
-                    }
-                    if (lane < BPC)
-                        tma_load_3d(smem + (size_t)s * a.stage_bytes + (kv * HALVES + half) * half_stride, &tmap,
-                                    &full[s], half * 64, row + kv * P, hg * Hc);
-                    row = row_next;
-                }
-            }
-        } else if (lane == 0) {
-            // several boxes per chunk (pages below 16 slots): once the slot frees, all the
-            // chunk's page ids (up to 16 at page size 1) are loaded together, then its boxes
-            // are issued (not one dependent load per box)
-            for (int ti = t_begin; ti < t_end; ++ti) {
-                const DecodeTile t = a.tiles[ti];
-                const ChunkRange cr = chunk_range(t, P);
-                bool ok = true;
-                for (int k = cr.k0; k < cr.nk; ++k, ++it) {
-                    const int s = it % a.stages;
-                    const uint32_t use = it / a.stages;
-                    if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, err, kErrWaitEmpty)) {
-                        ok = false;
-                        break;
-                    }
-                    const int pos0 = cr.base + k * kDecodeKeysPerStage;
-                    const int nbox = min(nb, (cr.end - pos0 + kpb - 1) / kpb);
-                    int page[kDecodeKeysPerStage];
-#pragma unroll
-                    for (int b = 0; b < kDecodeKeysPerStage; ++b)
-                        if (b < nbox) page[b] = a.pages[t.kv_base + ((pos0 + b * kpb) >> a.page_shift)];
-                    uint8_t *st = smem + (size_t)s * a.stage_bytes;
-                    mbar_arrive_expect_tx(&full[s], (uint32_t)(nbox * nkv * HALVES) * box_bytes);
-#pragma unroll
-                    for (int b = 0; b < kDecodeKeysPerStage; ++b)
-                        if (b < nbox) {
-                            const int row = page[b] * 2 * P + ((pos0 + b * kpb) & (P - 1));
-                            for (int kv = 0; kv < nkv; ++kv)
-#pragma unroll
-                                for (int h = 0; h < HALVES; ++h)
-                                    tma_load_3d(st + (kv * HALVES + h) * half_stride + b * a.box_stride, &tmap,
-                                                &full[s], h * 64, row + kv * P, hg * Hc);
-                        }
-                }
-                if (!ok) break;
-            }
-        }
-        // Drain: every stage issued must have been consumed before the CTA exits.
+        // ---------------- producer ----------------
         if (lane == 0) {
+            const int nkv = 2;
+            const uint32_t box_bytes = (uint32_t)a.box_rows * Hc * 128;
+            uint32_t it = 0;
+            if (!SMALL) {
+                // one box (of K and of V) per chunk: its page id is loaded after the slot frees
+                for (int ti = t_begin; ti < t_end; ++ti) {
+                    const DecodeTile t = a.tiles[ti];
+                    const ChunkRange cr = chunk_range(t, P);
+                    bool ok = true;
+                    for (int k = cr.k0; k < cr.nk; ++k, ++it) {
+                        const int s = it % a.stages;
+                        const uint32_t use = it / a.stages;
+                        if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, err, kErrWaitEmpty)) {
+                            ok = false;
+                            break;
+                        }
+                        const int pos0 = cr.base + k * kDecodeKeysPerStage;
+                        const int row = a.pages[t.kv_base + (pos0 >> a.page_shift)] * 2 * P + (pos0 & (P - 1));
+                        uint8_t *st = smem + (size_t)s * a.stage_bytes;
+                        mbar_arrive_expect_tx(&full[s], (uint32_t)(nkv * HALVES) * box_bytes);
+                        for (int kv = 0; kv < nkv; ++kv)
+#pragma unroll
+                            for (int h = 0; h < HALVES; ++h)
+                                tma_load_3d(st + (kv * HALVES + h) * half_stride, &tmap, &full[s], h * 64,
+                                            row + kv * P, hg * Hc);
+                    }
+                    if (!ok) break;
+                }
+            } else {
+                // several boxes per chunk (pages below 16 slots): once the slot frees, all the
+                // chunk's page ids (up to 16 at page size 1) are loaded together, then its boxes
+                // are issued (not one dependent load per box)
+                for (int ti = t_begin; ti < t_end; ++ti) {
+                    const DecodeTile t = a.tiles[ti];
+                    const ChunkRange cr = chunk_range(t, P);
+                    bool ok = true;
+                    for (int k = cr.k0; k < cr.nk; ++k, ++it) {
+                        const int s = it % a.stages;
+                        const uint32_t use = it / a.stages;
+                        if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, err, kErrWaitEmpty)) {
+                            ok = false;
+                            break;
+                        }
+                        const int pos0 = cr.base + k * kDecodeKeysPerStage;
+                        const int nbox = min(nb, (cr.end - pos0 + kpb - 1) / kpb);
+                        int page[kDecodeKeysPerStage];
+#pragma unroll
+                        for (int b = 0; b < kDecodeKeysPerStage; ++b)
+                            if (b < nbox) page[b] = a.pages[t.kv_base + ((pos0 + b * kpb) >> a.page_shift)];
+                        uint8_t *st = smem + (size_t)s * a.stage_bytes;
+                        mbar_arrive_expect_tx(&full[s], (uint32_t)(nbox * nkv * HALVES) * box_bytes);
+#pragma unroll
+                        for (int b = 0; b < kDecodeKeysPerStage; ++b)
+                            if (b < nbox) {
+                                const int row = page[b] * 2 * P + ((pos0 + b * kpb) & (P - 1));
+                                for (int kv = 0; kv < nkv; ++kv)
+#pragma unroll
+                                    for (int h = 0; h < HALVES; ++h)
+                                        tma_load_3d(st + (kv * HALVES + h) * half_stride + b * a.box_stride, &tmap,
+                                                    &full[s], h * 64, row + kv * P, hg * Hc);
+                            }
+                    }
+                    if (!ok) break;
+                }
+            }
+            // Drain: every stage issued must have been consumed before the CTA exits.
             const uint32_t issued = it;
             for (uint32_t d = issued > (uint32_t)a.stages ? issued - a.stages : 0; d < issued; ++d) {
                 const int s = d % a.stages;
