@@ -480,7 +480,7 @@ def l2_flush_buffer(dev):
     return L2Flush(dev)
 
 
-def time_runs(fn, flush, iters=10, warm=3):
+def time_runs(fn, flush, iters=20, warm=3):
     for _ in range(warm):
         fn()
     torch.cuda.synchronize()
