@@ -13,8 +13,10 @@ CSRC = os.path.join(PKG, "csrc")
 ROOT = os.path.dirname(PKG)
 OUT = os.path.join(PKG, "libpkv.so")
 OBJ = os.path.join(PKG, "_build")
-SOURCES = ["pkv_api.cu", "decode.cu", "prefill.cu", "prefill_gather.cu", "prefill_pair.cu", "planner.cpp"]
-HEADERS = ["plan.h", "launch.h", "ptx.cuh", "tcgen05.cuh", "prefill_kernel.cuh", "prefill_pair.cuh"]
+SOURCES = ["pkv_api.cu", "decode.cu", "prefill.cu", "prefill_gather.cu", "prefill_pair.cu", "prefill_wide.cu",
+           "planner.cpp"]
+HEADERS = ["plan.h", "launch.h", "ptx.cuh", "tcgen05.cuh", "prefill_kernel.cuh", "prefill_pair.cuh",
+           "prefill_wide.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

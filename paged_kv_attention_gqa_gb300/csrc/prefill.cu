@@ -1,6 +1,7 @@
 // Ragged paged prefill launcher (FlashInferPrefillWrapper.run, FlashInferMixedWrapper's
-// prefill pass, DenseAttentionManager): picks the kernel instance of prefill_kernel.cuh for
-// the shape; pages below 8 slots go to the cp.async-gather instances in prefill_gather.cu.
+// prefill pass, DenseAttentionManager): head_dim 64 / 128 with K / V by TMA go to the
+// two-query-tile kernel (prefill_pair.cuh), head_dim 256 by TMA to prefill_wide.cuh, pages
+// below 8 slots to the cp.async-gather instances of prefill_kernel.cuh (prefill_gather.cu).
 #include "../../include/pkv.h"
 #include "prefill_kernel.cuh"
 
@@ -45,6 +46,8 @@ cudaError_t launch_prefill(const Shape &s, const Plan &p, const CUtensorMap &tm_
         return launch_prefill_pair(s.head_dim, g, tm_kv, tm_v, tm_q, a, grid, st);
     if (a.gather && p.mode != PKV_MODE_DENSE)  // dense plans always read K / V by TMA
         return launch_prefill_gather(s.head_dim, g, tm_kv, tm_v, tm_q, a, grid, smem, st);
+    if (s.head_dim == 256)  // 128-key tiles, two S buffers (prefill_wide.cuh)
+        return launch_prefill_wide(g, tm_kv, tm_v, tm_q, a, grid, st);
 #define PKV_PF(DD, GG) \
     if (s.head_dim == DD && g == GG) e = launch_prefill_t<DD, GG, false>(tm_kv, tm_v, tm_q, a, grid, smem, st);
     PKV_FOR_EACH_HEAD_DIM_AND_GROUP(PKV_PF)

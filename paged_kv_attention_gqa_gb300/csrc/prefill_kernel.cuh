@@ -493,6 +493,9 @@ __global__ void __launch_bounds__(GATHER ? kPfGatherThreads : kPfThreads, D > 12
 // Two query tiles per CTA, head_dim 64 / 128 read by TMA: prefill_pair.cu.
 cudaError_t launch_prefill_pair(int head_dim, int group, const CUtensorMap &tkv, const CUtensorMap &tv,
                                 const CUtensorMap &tq, const dev::PrefillArgs &a, int grid, cudaStream_t st);
+// One query tile per CTA with two S buffers, head_dim 256 read by TMA: prefill_wide.cu.
+cudaError_t launch_prefill_wide(int group, const CUtensorMap &tkv, const CUtensorMap &tv, const CUtensorMap &tq,
+                                const dev::PrefillArgs &a, int grid, cudaStream_t st);
 // Instances with GATHER = true live in prefill_gather.cu (compiled in parallel).
 cudaError_t launch_prefill_gather(int head_dim, int group, const CUtensorMap &tkv, const CUtensorMap &tv,
                                   const CUtensorMap &tq, const dev::PrefillArgs &a, int grid, size_t smem,
