@@ -12,7 +12,8 @@
 // shared memory, all 512 tensor-memory columns):
 //  * warp 4 loads Q once and streams the 128-key K tiles, warp 5 the V tiles (TMA boxes of 16 or 8
 //    slots of the kv head, 64-column quarters, 128-byte swizzle; one lane per box, its page looked
-//    up a tile ahead), one stage each (a tile of 128 keys x 256 columns is 64 KB);
+//    up a tile ahead), one stage each (a tile of 128 keys x 256 columns is 64 KB); the K stage is
+//    refilled quarter by quarter as S(j)'s k-steps release them;
 //  * tensor memory holds two S buffers of 128 fp32 columns (P written over each as bf16) and O
 //    (256 fp32 columns).  Warp 6 issues S(j) = Q K_j^T (N = 128: both operands in shared memory at
 //    the full MMA rate) into buffer j % 2 once PV(j-2), which read P(j-2) from it, completed; warp
@@ -45,7 +46,7 @@ struct PwSmem {
     static constexpr uint32_t K_OFF = Q_TILE;
     static constexpr uint32_t V_OFF = K_OFF + KV_TILE;
     static constexpr uint32_t BAR_OFF = V_OFF + KV_TILE;
-    static constexpr uint32_t BYTES = BAR_OFF + 128;
+    static constexpr uint32_t BYTES = BAR_OFF + 256;
 };
 
 // A shared-memory descriptor for base + off: the base's plus off >> 4 in the start-address field
@@ -61,22 +62,23 @@ __global__ void __launch_bounds__(kPwThreads, 1)
     constexpr int QUARTERS = L::QUARTERS;
     constexpr int BQ = kPrefillRowsPerTile / G;          // tokens per query tile
     constexpr uint32_t Q_TX = (uint32_t)BQ * G * D * 2;  // rows BQ*G..127 stay unused
-    constexpr int KSTEPS = D / 16;                       // k-steps of S = Q K^T
     constexpr int PSTEPS = kPwKeys / 16;                 // k-steps of O += P V
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::BAR_OFF);
     // K / V stages, S / P buffers and PV completions: once per K/V tile (q_full, o_final once)
+    // The K stage is filled and released by 64-column quarter: S(j)'s k-steps read the quarters in
+    // turn, so quarter q of K(j+1) is requested once the MMAs reading quarter q of K(j) completed.
     uint64_t *q_full = bars + 0;
-    uint64_t *k_full = bars + 1;
-    uint64_t *k_empty = bars + 2;   // the S MMAs reading the K stage completed
-    uint64_t *v_full = bars + 3;
-    uint64_t *v_empty = bars + 4;   // the PV MMAs reading the V stage completed
-    uint64_t *s_full = bars + 5;    // [2] S(j) in buffer j % 2
-    uint64_t *p_full = bars + 7;    // [2] P(j) written over buffer j % 2 (and O rescaled if it had to be)
-    uint64_t *pv_done = bars + 9;   // [2] PV(j) completed, counted on buffer j % 2
-    uint64_t *o_final = bars + 11;  // the last PV completed
-    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 12);
+    uint64_t *k_full = bars + 1;    // [4] a quarter of K(j) landed
+    uint64_t *k_empty = bars + 5;   // [4] the S MMAs reading a quarter of K(j) completed
+    uint64_t *v_full = bars + 9;
+    uint64_t *v_empty = bars + 10;  // the PV MMAs reading the V stage completed
+    uint64_t *s_full = bars + 11;   // [2] S(j) in buffer j % 2
+    uint64_t *p_full = bars + 13;   // [2] P(j) written over buffer j % 2 (and O rescaled if it had to be)
+    uint64_t *pv_done = bars + 15;  // [2] PV(j) completed, counted on buffer j % 2
+    uint64_t *o_final = bars + 17;  // the last PV completed
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 18);
 
     if ((int)blockIdx.x >= a.hdr->pf_tiles) return;  // an idle CTA of a launch at the maxima
     const PrefillTile t = a.tiles[blockIdx.x];
@@ -92,8 +94,10 @@ __global__ void __launch_bounds__(kPwThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        mbar_init(k_full, 1);
-        mbar_init(k_empty, 1);
+        for (int q = 0; q < QUARTERS; ++q) {
+            mbar_init(&k_full[q], 1);
+            mbar_init(&k_empty[q], 1);
+        }
         mbar_init(v_full, 1);
         mbar_init(v_empty, 1);
         for (int b = 0; b < 2; ++b) {
@@ -144,8 +148,6 @@ __global__ void __launch_bounds__(kPwThreads, 1)
         // A 128-key tile is NB boxes of R = 128 / NB rows (16, or 8 for 8-slot pages); lane b < NB
         // copies box b (its four 64-column quarters) and looks up the box's page one tile ahead.
         const int kv = warp == 5;
-        uint64_t *full = kv ? v_full : k_full;
-        uint64_t *empty = kv ? v_empty : k_empty;
         uint8_t *stage = sm + (kv ? L::V_OFF : L::K_OFF);
         const int NB = (dense || a.box_rows == 16) ? 8 : 16;
         const int R = kPwKeys / NB;
@@ -162,17 +164,33 @@ __global__ void __launch_bounds__(kPwThreads, 1)
                        : a.oob_row;
         };
         int row = (lane < NB && nt > 0) ? box_row(0) : 0;
-        for (int j = 0; j < nt; ++j) {
-            // the MMAs that read the stage's previous tile must have completed
-            if (j > 0 && !mbar_wait(empty, (j - 1) & 1, err, kErrWaitEmpty)) break;
-            if (lane == 0) mbar_arrive_expect_tx(full, L::KV_TILE);
-            __syncwarp();
-            if (lane < NB) {
+        bool ok = true;
+        for (int j = 0; j < nt && ok; ++j) {
+            if (kv) {
+                // the PV MMAs that read the stage's previous tile must have completed
+                if (j > 0 && !mbar_wait(v_empty, (j - 1) & 1, err, kErrWaitEmpty)) break;
+                if (lane == 0) mbar_arrive_expect_tx(v_full, L::KV_TILE);
+                __syncwarp();
+                if (lane < NB) {
 #pragma unroll
-                for (int h = 0; h < QUARTERS; ++h)
-                    tma_load_3d(stage + h * L::KV_QUARTER + lane * R * 128, map, full, h * 64, row, t.kv_head);
-                if (j + 1 < nt) row = box_row(j + 1);  // lands while the stage is awaited
+                    for (int h = 0; h < QUARTERS; ++h)
+                        tma_load_3d(stage + h * L::KV_QUARTER + lane * R * 128, map, v_full, h * 64, row, t.kv_head);
+                }
+            } else {
+                for (int h = 0; h < QUARTERS; ++h) {
+                    // the S MMAs that read this quarter of the previous tile must have completed
+                    if (j > 0 && !mbar_wait(&k_empty[h], (j - 1) & 1, err, kErrWaitEmpty)) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0) mbar_arrive_expect_tx(&k_full[h], L::KV_QUARTER);
+                    __syncwarp();
+                    if (lane < NB)
+                        tma_load_3d(stage + h * L::KV_QUARTER + lane * R * 128, map, &k_full[h], h * 64, row,
+                                    t.kv_head);
+                }
             }
+            if (lane < NB && j + 1 < nt) row = box_row(j + 1);  // lands while the stage is awaited
         }
     } else if (warp == 6) {
         // ------------------------------------------------ S(j) = Q K_j^T into buffer j % 2
@@ -183,17 +201,20 @@ __global__ void __launch_bounds__(kPwThreads, 1)
         bool ok = mbar_wait(q_full, 0, err, kErrWaitFull);
         for (int j = 0; j < nt && ok; ++j) {
             const int b = j & 1;
-            ok = mbar_wait(k_full, j & 1, err, kErrWaitFull);
-            // buffer b holds P(j-2) until PV(j-2) completed (its next phase, PV(j), needs S(j))
-            if (ok && j >= 2) ok = mbar_wait(&pv_done[b], ((j - 2) >> 1) & 1, err, kErrWaitFull);
-            if (!ok) break;
-            tc_fence_after();
+#pragma unroll 1
+            for (int h = 0; h < QUARTERS && ok; ++h) {
+                ok = mbar_wait(&k_full[h], j & 1, err, kErrWaitFull);
+                // buffer b holds P(j-2) until PV(j-2) completed (its next phase, PV(j), needs S(j))
+                if (ok && h == 0 && j >= 2) ok = mbar_wait(&pv_done[b], ((j - 2) >> 1) & 1, err, kErrWaitFull);
+                if (!ok) break;
+                tc_fence_after();
 #pragma unroll
-            for (int kk = 0; kk < KSTEPS; ++kk)
-                mma_ss_elect(tmem + 128u * (uint32_t)b, pw_desc(dQ, (kk / 4) * L::Q_QUARTER + (kk % 4) * 32),
-                             pw_desc(dK, (kk / 4) * L::KV_QUARTER + (kk % 4) * 32), ID_S, kk > 0 ? 1u : 0u);
-            mma_commit_elect(&s_full[b]);
-            mma_commit_elect(k_empty);  // K_j's stage frees once these MMAs completed
+                for (int kk = 4 * h; kk < 4 * h + 4; ++kk)
+                    mma_ss_elect(tmem + 128u * (uint32_t)b, pw_desc(dQ, (kk / 4) * L::Q_QUARTER + (kk % 4) * 32),
+                                 pw_desc(dK, (kk / 4) * L::KV_QUARTER + (kk % 4) * 32), ID_S, kk > 0 ? 1u : 0u);
+                mma_commit_elect(&k_empty[h]);  // this quarter of K_j frees once these MMAs completed
+            }
+            if (ok) mma_commit_elect(&s_full[b]);
         }
     } else if (warp == 7) {
         // ------------------------------------------------ O += P(j) V_j

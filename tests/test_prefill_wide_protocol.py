@@ -4,7 +4,9 @@ producer warps, its two MMA-issuing warps (one for S = Q K^T, one for O += P V) 
 warps under random latencies, with waits that poll by parity exactly as `mbarrier.try_wait.parity`
 does.
 
-The kernel's barriers: q_full; k_full / k_empty and v_full / v_empty (one stage each for K and V);
+The kernel's barriers: q_full; k_full[4] / k_empty[4] (one K stage, filled and released by 64-column
+quarter: S(j)'s k-steps read the quarters in turn, so quarter q of K(j+1) is requested as soon as
+the MMAs reading quarter q of K(j) completed); v_full / v_empty (one V stage);
 s_full[2] (S(j) done in tensor-memory buffer j % 2), p_full[2] (the four softmax warps wrote P(j)
 over that buffer), pv_done[2] (PV(j) done, counted per buffer), o_final. A commit makes its barrier
 arrive once every MMA its own warp issued before it has completed.
@@ -19,8 +21,8 @@ Checked under many random schedules:
     rescaled only while no PV is in flight; the epilogue reads O after all PVs;
   * every actor finishes (no deadlock).
 Planted mistakes -- S(j) issued without waiting for PV(j-2), one pv_done barrier for both buffers
-(waited two phases back), PV issued without waiting for P, the tail rows not zeroed first -- are
-caught."""
+(waited two phases back), PV issued without waiting for P, the tail rows not zeroed first, every K
+quarter refilled on the first quarter's release -- are caught."""
 import heapq
 import random
 
@@ -36,7 +38,8 @@ class Sim:
         self.t, self.seq, self.q = 0, 0, []
         B = Barrier
         self.q_full = B("q_full", 1)
-        self.k_full, self.k_empty = B("k_full", 1), B("k_empty", 1)
+        self.k_full = [B(f"k_full{q}", 1) for q in range(4)]
+        self.k_empty = [B(f"k_empty{q}", 1) for q in range(4)]
         self.v_full, self.v_empty = B("v_full", 1), B("v_empty", 1)
         self.s_full = [B(f"s_full{b}", 1) for b in range(2)]
         self.p_full = [B(f"p_full{b}", 4) for b in range(2)]
@@ -89,36 +92,41 @@ class Sim:
     def producer(self, kv):
         if kv == 0:
             self.q_full.arrive(self)
-        full, empty, name = (self.k_full, self.k_empty, "K") if kv == 0 else (self.v_full, self.v_empty, "V")
+        parts = range(4) if kv == 0 else [None]
         for j in range(self.nt):
-            if j > 0:
-                yield ("wait", empty, j - 1)
-                late = [c for c in self.readers.get((name, j - 1), []) if c > self.t]
-                assert not late, f"{name} stage refilled with tile {j} while an MMA still reads tile {j - 1}"
-            land = self.t + self.rng.randint(10, 2000)
+            for q in parts:
+                full = self.k_full[q] if kv == 0 else self.v_full
+                empty = self.k_empty[q if self.plant != "k_single_release" else 0] if kv == 0 else self.v_empty
+                key = ("K", j, q) if kv == 0 else ("V", j)
+                prev = ("K", j - 1, q) if kv == 0 else ("V", j - 1)
+                if j > 0:
+                    yield ("wait", empty, j - 1)
+                    late = [c for c in self.readers.get(prev, []) if c > self.t]
+                    assert not late, f"stage part {key} refilled while an MMA still reads {prev}"
 
-            def fire(key=(name, j)):
-                self.land[key] = self.t
-                full.arrive(self)
-            self.later(land - self.t, fire)
-            yield ("delay", self.rng.randint(0, 60))
+                def fire(key=key, full=full):
+                    self.land[key] = self.t
+                    full.arrive(self)
+                self.later(self.rng.randint(10, 2000), fire)
+                yield ("delay", self.rng.randint(0, 60))
 
     def s_issuer(self):
         yield ("wait", self.q_full, 0)
         for j in range(self.nt):
-            yield ("wait", self.k_full, j)
-            if j >= 2 and self.plant != "no_buf_wait":
-                if self.plant == "single_pv_barrier":
-                    yield ("wait", self.pv_one, j - 2)
-                else:
-                    yield ("wait", self.pv_done[j % 2], (j - 2) // 2)
-            if j >= 2:
-                assert self.pv_cpl.get(j - 2, 1 << 60) <= self.t, f"S({j}) issued while PV({j - 2}) reads its buffer"
-            assert self.land.get(("K", j), 1 << 60) <= self.t, f"S({j}) before K_{j} landed"
-            self.s_cpl[j] = self.issue("s", ("K", j))
+            for q in range(4):  # the k-steps of quarter q, then its release
+                yield ("wait", self.k_full[q], j)
+                if q == 0 and j >= 2 and self.plant != "no_buf_wait":
+                    if self.plant == "single_pv_barrier":
+                        yield ("wait", self.pv_one, j - 2)
+                    else:
+                        yield ("wait", self.pv_done[j % 2], (j - 2) // 2)
+                if q == 0 and j >= 2:
+                    assert self.pv_cpl.get(j - 2, 1 << 60) <= self.t, f"S({j}) issued while PV({j - 2}) reads its buffer"
+                assert self.land.get(("K", j, q), 1 << 60) <= self.t, f"S({j}) quarter {q} before it landed"
+                self.s_cpl[j] = self.issue("s", ("K", j, q))
+                self.commit("s", self.k_empty[q])
+                yield ("delay", self.rng.randint(1, 40))
             self.commit("s", self.s_full[j % 2])
-            self.commit("s", self.k_empty)
-            yield ("delay", self.rng.randint(1, 40))
 
     def pv_issuer(self):
         for j in range(self.nt):
@@ -176,7 +184,7 @@ def test_wide_barrier_protocol_is_sound(nt):
         Sim(nt, seed * 1000 + nt, tail=bool(seed & 1)).run()
 
 
-@pytest.mark.parametrize("plant", ["no_buf_wait", "single_pv_barrier", "no_p_wait", "no_tail"])
+@pytest.mark.parametrize("plant", ["no_buf_wait", "single_pv_barrier", "no_p_wait", "no_tail", "k_single_release"])
 def test_wide_model_catches_a_broken_protocol(plant):
     caught = 0
     for seed in range(200):
