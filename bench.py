@@ -55,6 +55,8 @@ def parse():
     ap.add_argument("--separate-append", action="store_true",
                     help="decode workloads: pkv_kv_append_planned + pkv_run_decode per layer instead of the fused call")
     ap.add_argument("--layers", type=int, default=0, help="fewer cache layers (profiling a small case)")
+    ap.add_argument("--heads", default=None,
+                    help="Hq/Hkv/head_dim for --config prefill (the same lengths on another head shape, e.g. 16/8/256)")
     return ap.parse_args()
 
 
@@ -408,6 +410,10 @@ def run_step_primary(args, rank, world):
     stream = torch.cuda.current_stream()
     peaks = measured_peaks()
     pb = wl.config_prefill(seed=args.seed) if args.config == "prefill" else wl.config_mixed(seed=args.seed)
+    if args.config == "prefill" and args.heads:
+        hq, hkv, d = (int(v) for v in args.heads.split("/"))
+        pb = wl.custom(args.seed, pb.kv_lens, pb.qo_lens, num_qo_heads=hq, num_kv_heads=hkv, head_dim=d,
+                       page_size=pb.page_size)
     mode = B.MODE_PREFILL if args.config == "prefill" else B.MODE_MIXED
     x = wl.make_inputs(pb, device=dev, seed=args.seed, unused="randn")
     kv = x["kv_cache"][0]
@@ -438,10 +444,12 @@ def run_step_primary(args, rank, world):
         fl = prefill_flops(pb)
         value, unit = world * fl / (ms * 1e-3) / 1e12, "TFLOP/s"
         achieved = fl / (kms * 1e-3) / 1e12
+        wide = pb.head_dim == 256
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": round(achieved / peaks["bf16_tflops"], 4),
-                "traffic": kernel_traffic("prefill_pair.cuh", "prefill_ragged16_pair.md"),
-                "kernel": "prefill_pair_kernel",
+                "traffic": (kernel_traffic("prefill_wide.cuh", "prefill_ragged16_d256.md") if wide
+                            else kernel_traffic("prefill_pair.cuh", "prefill_ragged16_pair.md")),
+                "kernel": "prefill_wide_kernel" if wide else "prefill_pair_kernel",
                 "launch_ms": round(kms, 5), "peak_source": peaks["source"]}
         launches = 2
     else:
