@@ -7,15 +7,15 @@
 
 namespace pkv {
 size_t prefill_smem_bytes(const Shape &s) {
-    // at least 100 KB, so that no more than two CTAs (2 x 256 TMEM columns) share an SM;
-    // head_dim 256 (512 columns) takes more than half an SM's shared memory
+    // the cp.async-gather kernel: at least 100 KB, so that no more than two CTAs (2 x 256 TMEM
+    // columns) share an SM; head_dim 256 (512 columns) takes more than half an SM's shared memory
     const size_t need = 1024 + (s.head_dim == 64    ? dev::PfSmem<64>::BYTES
                                 : s.head_dim == 128 ? dev::PfSmem<128>::BYTES
                                                     : dev::PfSmem<256>::BYTES);
     return need < 100 * 1024 ? 100 * 1024 : need;
 }
-static_assert(1024 + dev::PfSmem<256>::BYTES > 228 * 1024 / 2, "one head_dim-256 prefill CTA per SM");
-static_assert(1024 + dev::PfSmem<256>::BYTES <= 227 * 1024, "head_dim-256 prefill fits shared memory");
+static_assert(1024 + dev::PfSmem<256>::BYTES > 228 * 1024 / 2, "one head_dim-256 gather-prefill CTA per SM");
+static_assert(1024 + dev::PfSmem<256>::BYTES <= 227 * 1024, "the head_dim-256 gather prefill fits shared memory");
 
 cudaError_t launch_prefill(const Shape &s, const Plan &p, const CUtensorMap &tm_kv, const CUtensorMap &tm_v,
                            const CUtensorMap &tm_q, const void *kv_layer, void *ws, void *out, float *lse,
@@ -39,20 +39,14 @@ cudaError_t launch_prefill(const Shape &s, const Plan &p, const CUtensorMap &tm_
     if (a.gather && p.mode != PKV_MODE_DENSE && !kv_layer) return cudaErrorInvalidValue;
     // a row coordinate past the tensor (TMA fills zeros); dense plans never use it
     a.oob_row = s.num_cache_pages * 2 * s.page_size;
-    const size_t smem = prefill_smem_bytes(s);
-    cudaError_t e = cudaErrorInvalidValue;
     const int g = s.group();
     if (s.pf_pair(p.mode == PKV_MODE_DENSE))  // two query tiles per CTA (prefill_pair.cuh)
         return launch_prefill_pair(s.head_dim, g, tm_kv, tm_v, tm_q, a, grid, st);
     if (a.gather && p.mode != PKV_MODE_DENSE)  // dense plans always read K / V by TMA
-        return launch_prefill_gather(s.head_dim, g, tm_kv, tm_v, tm_q, a, grid, smem, st);
+        return launch_prefill_gather(s.head_dim, g, tm_kv, tm_v, tm_q, a, grid, prefill_smem_bytes(s), st);
     if (s.head_dim == 256)  // 128-key tiles, two S buffers (prefill_wide.cuh)
         return launch_prefill_wide(g, tm_kv, tm_v, tm_q, a, grid, st);
-#define PKV_PF(DD, GG) \
-    if (s.head_dim == DD && g == GG) e = launch_prefill_t<DD, GG, false>(tm_kv, tm_v, tm_q, a, grid, smem, st);
-    PKV_FOR_EACH_HEAD_DIM_AND_GROUP(PKV_PF)
-#undef PKV_PF
-    return e;
+    return cudaErrorInvalidValue;  // every shape pkv_create accepts is taken above
 }
 
 }  // namespace pkv
