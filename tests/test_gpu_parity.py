@@ -304,13 +304,14 @@ def test_nvtx_handle_gives_bit_identical_results(mode):
 
 # ------------------------------------------------------------------ context-only attention (causal = 2)
 
+@pytest.mark.parametrize("heads", [(32, 8, 128), (16, 8, 256)])
 @pytest.mark.parametrize("window", [-1, 0, 5, 100])
-def test_prefill_context_only(window):
+def test_prefill_context_only(window, heads):
     import oracle_pins
     from paged_kv_attention_gqa_gb300 import binding as B
     L = [0, 37, 16, 300, 5, 129, 64]
     n = [3, 10, 40, 64, 70, 1, 130]
-    pb = wl.custom(60, L, n, num_qo_heads=32, num_kv_heads=8, head_dim=128, page_size=16)
+    pb = wl.custom(60, L, n, num_qo_heads=heads[0], num_kv_heads=heads[1], head_dim=heads[2], page_size=16)
     q, kv = oracle_pins.context_step(pb, seed=3)
     x = dict(q=q.cuda(), k_new=None, v_new=None, kv_cache=kv.unsqueeze(0).cuda())
     out, lse, h, ws = G.gpu_step(pb, x, "prefill", causal=B.CONTEXT_ONLY, window_left=window, append=False)
@@ -321,7 +322,7 @@ def test_prefill_context_only(window):
     assert np.all(o[np.broadcast_to(empty[..., None], o.shape)] == 0)
     ref_l = np.where(empty, 0, ref_l)
     l_cmp = torch.from_numpy(np.where(empty, 0, l))
-    G.compare(out, l_cmp, ref_o, ref_l, what=f"context-only window {window}")
+    G.compare(out, l_cmp, ref_o, ref_l, what=f"context-only window {window} D{heads[2]}")
 
 
 def test_context_only_views_then_prefill_matches_full_rows_without_their_queries():

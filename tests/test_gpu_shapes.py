@@ -178,6 +178,14 @@ def test_prefill_head_dim_256(Hq, Hkv, causal):
     _check_step(pb, "prefill", causal=causal, seed=7)
 
 
+@pytest.mark.parametrize("window", [0, 5, 100, 200])
+def test_prefill_head_dim_256_window(window):
+    n = [1, 7, 33, 130, 300]
+    c = [0, 40, 0, 300, 900]
+    pb = wl.custom(162, np.add(n, c), n, num_qo_heads=16, num_kv_heads=8, head_dim=256, page_size=16)
+    _check_step(pb, "prefill", window_left=window, seed=8)
+
+
 # ------------------------------------------------------------------ group sizes 3, 5, 6, 7
 
 @pytest.mark.parametrize("g", [3, 5, 6, 7])
