@@ -505,8 +505,8 @@ def time_runs(fn, flush, iters=20, warm=3):
 
 
 def secondary(B, dev, peaks, seed):
-    """Prefill (TFLOP/s vs bf16 peak), mixed step and long-context decode, each timed per
-    call with an L2 flush between calls."""
+    """Prefill (TFLOP/s vs bf16 peak), mixed step, the batch workload's append and long-context
+    decode, each timed per call with an L2 flush between calls."""
     res = {}
     flush = l2_flush_buffer(dev)
     # ragged causal prefill with cached prefix
@@ -552,6 +552,22 @@ def secondary(B, dev, peaks, seed):
     res["mixed"] = {"workload": "96 decode rows + 4 prompt rows, 32/8/128", "ms": round(ms, 4),
                     "roofline_ms": round(bound_ms, 4), "frac": round(bound_ms / ms, 4),
                     "decode_kv_gb": round(dec_bytes / 1e9, 3), "prefill_tflop": round(pf_fl / 1e12, 4)}
+    del x, kv
+    # the batch-decode workload's append of its 128 new tokens into one layer slice, alone:
+    # at the plan's write locations, and from device index arrays (no plan)
+    pb = wl.config_batch_decode(seed=seed, num_layers=1)
+    x = wl.make_inputs(pb, device=dev, seed=seed, unused="randn", layers=1)
+    h = make_handle(pb, B)
+    ws = torch.empty(h.workspace_size(B.MODE_DECODE), dtype=torch.uint8, device=dev)
+    h.plan(B.MODE_DECODE, None, pb.kv_indptr, pb.kv_indices, pb.last_page_len, workspace=ws)
+    kv = x["kv_cache"][0]
+    idx = [torch.as_tensor(np.asarray(a, np.int32), device=dev) for a in (pb.kv_indptr, pb.kv_indices, pb.last_page_len)]
+    planned_ms = time_runs(lambda: h.kv_append_planned(x["k_new"], x["v_new"], kv, workspace=ws), flush)
+    indexed_ms = time_runs(lambda: h.kv_append(x["k_new"], x["v_new"], pb.batch, kv, None, *idx, pb.batch), flush)
+    app_bytes = 2 * pb.batch * pb.num_kv_heads * pb.head_dim * 2 * 2  # K and V rows read and written
+    res["append_batch"] = {"workload": "128 new tokens (one per row) into one layer slice, 8 kv heads, head_dim 128",
+                           "planned_us": round(planned_ms * 1e3, 2), "indexed_us": round(indexed_ms * 1e3, 2),
+                           "bytes": app_bytes}
     del x, kv
     # long-context split-KV decode, full and windowed
     for window in (-1, 4096):
