@@ -356,10 +356,11 @@ static void prefill_tiles(const Shape &s, const std::vector<int> &rows, const in
 }
 
 // Time model of one GB300 used to share the SMs between the two passes of a mixed step:
-// streaming K/V at ~6.4 TB/s, prefill tiles at ~0.9 PFLOP/s (both measured on this
-// library's own kernels; the flops count every query row of a tile).
+// streaming K/V at ~6.4 TB/s, prefill tiles at 0.7 PFLOP/s (the flops count every query row
+// and key of a tile, masked ones included; the rate is the one that gave the shortest step
+// when the two passes share the GPU, between 0.3 and 2.5 PFLOP/s on the 96 + 4 row step).
 constexpr double kDecodeBytesPerUs = 6.4e6;
-constexpr double kPrefillFlopsPerUs = 0.9e9;
+constexpr double kPrefillFlopsPerUs = 0.7e9;
 
 static int mixed_decode_ctas(const Shape &s, int rows, const int32_t *kvp, const int32_t *lpl, int window_left,
                              const std::vector<PrefillTile> &ptiles) {
