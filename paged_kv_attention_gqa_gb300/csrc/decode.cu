@@ -174,7 +174,21 @@ __global__ void __launch_bounds__((D > 128 ? 4 + (SMALL ? 2 : 1) : 8 + (SMALL ? 
         prefetch_tmap(&tmap);
     }
     __syncthreads();
-    griddep_wait();  // inputs, the cache and the merge counters may come from the previous kernel
+    // The plan's arrays come from the host's copy, never from a kernel: the TMA producer reads its
+    // first tile and page id before waiting for the previous kernel, so those dependent loads
+    // overlap that kernel's tail.  Inputs, the cache and the merge counters may come from the
+    // previous kernel and are read only after the wait.
+    DecodeTile first_tile{};
+    int first_row = -1;
+    if (!SMALL && warp == Hc && lane == 0) {
+        first_tile = a.tiles[t_begin];
+        const ChunkRange cr = chunk_range(first_tile, P);
+        if (cr.k0 < cr.nk) {
+            const int pos0 = cr.base + cr.k0 * kDecodeKeysPerStage;
+            first_row = a.pages[first_tile.kv_base + (pos0 >> a.page_shift)] * 2 * P + (pos0 & (P - 1));
+        }
+    }
+    griddep_wait();
     griddep_launch();
 
     if (SMALL && a.gather && warp >= Hc) {
@@ -250,7 +264,7 @@ __global__ void __launch_bounds__((D > 128 ? 4 + (SMALL ? 2 : 1) : 8 + (SMALL ? 
             if (!SMALL) {
                 // one box (of K and of V) per chunk: its page id is loaded after the slot frees
                 for (int ti = t_begin; ti < t_end; ++ti) {
-                    const DecodeTile t = a.tiles[ti];
+                    const DecodeTile t = ti == t_begin ? first_tile : a.tiles[ti];
                     const ChunkRange cr = chunk_range(t, P);
                     bool ok = true;
                     for (int k = cr.k0; k < cr.nk; ++k, ++it) {
@@ -261,7 +275,9 @@ __global__ void __launch_bounds__((D > 128 ? 4 + (SMALL ? 2 : 1) : 8 + (SMALL ? 
                             break;
                         }
                         const int pos0 = cr.base + k * kDecodeKeysPerStage;
-                        const int row = a.pages[t.kv_base + (pos0 >> a.page_shift)] * 2 * P + (pos0 & (P - 1));
+                        const int row = ti == t_begin && k == cr.k0
+                                            ? first_row
+                                            : a.pages[t.kv_base + (pos0 >> a.page_shift)] * 2 * P + (pos0 & (P - 1));
                         uint8_t *st = smem + (size_t)s * a.stage_bytes;
                         mbar_arrive_expect_tx(&full[s], (uint32_t)(nkv * HALVES) * box_bytes);
                         for (int kv = 0; kv < nkv; ++kv)
