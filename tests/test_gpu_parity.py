@@ -122,6 +122,23 @@ def test_decode_page_pool_permutation_is_bit_identical():
     assert torch.equal(lse1, lse2)
 
 
+@pytest.mark.parametrize("heads", [(32, 8, 128), (16, 8, 256)])
+def test_prefill_page_pool_permutation_is_bit_identical(heads):
+    """The plan depends only on the lengths, so relabelling and moving the pool's pages leaves
+    every output bit unchanged (the two-query-tile kernel at head_dim 128, the head_dim-256
+    kernel)."""
+    import oracle_pins
+    pb = wl.custom(17, [300, 17, 1000, 64, 200], [40, 17, 300, 1, 129], num_qo_heads=heads[0],
+                   num_kv_heads=heads[1], head_dim=heads[2], page_size=16, pool_factor=1.5)
+    x = wl.make_inputs(pb, device="cuda", seed=15, unused="nan", layers=1)
+    out1, lse1, _, _ = G.gpu_step(pb, x, "prefill")
+    pb2, kv2 = oracle_pins.relabel_pool(pb, x["kv_cache"][0], seed=19)
+    x2 = dict(x, kv_cache=kv2.unsqueeze(0))
+    out2, lse2, _, _ = G.gpu_step(pb2, x2, "prefill", append=False)
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(lse1, lse2)
+
+
 def test_empty_batch_is_a_no_op():
     pb = wl.custom(8, [5], [1], num_qo_heads=8, num_kv_heads=2, head_dim=64, page_size=16)
     h = G.make_handle(pb)
