@@ -365,6 +365,18 @@ pkv_status pkv_context_only_views(int page_size, const int32_t *qo_indptr, const
 pkv_status pkv_decode_split(pkv_handle_t h, const int32_t *paged_kv_indptr, const int32_t *paged_kv_last_page_len,
                             int batch, int window_left, int32_t *tiles, int *num_tiles, int *num_ctas);
 
+/*
+ * The cache rows (page id * 2 * page_size + slot) of the first 4 16-key chunks of each
+ * decode CTA of that split, in the order the CTA reads them, -1 past its last chunk: the
+ * values the plan stores beside each CTA's tile range, from which the CTA's first K / V
+ * copies are issued without loading its tile and page ids first.  rows holds 4 * capacity
+ * ints; *num_ctas in: capacity (CTAs), out: CTAs written.  Host only.  PKV_ERR_INVALID on a
+ * null argument or a buffer below the CTA count.
+ */
+pkv_status pkv_decode_head_rows(pkv_handle_t h, const int32_t *paged_kv_indptr, const int32_t *paged_kv_indices,
+                                const int32_t *paged_kv_last_page_len, int batch, int window_left, int32_t *rows,
+                                int *num_ctas);
+
 #ifdef __cplusplus
 }
 #endif

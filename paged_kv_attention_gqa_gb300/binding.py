@@ -23,7 +23,7 @@ STATUS_NAMES = ["OK", "INVALID", "UNSUPPORTED", "WORKSPACE", "TOO_MANY_PREFILL_R
 # every symbol include/pkv.h declares
 EXPORTS = ["pkv_create", "pkv_destroy", "pkv_last_error", "pkv_workspace_size", "pkv_plan", "pkv_kv_append", "pkv_kv_append_planned",
            "pkv_run_decode", "pkv_run_prefill", "pkv_run_mixed", "pkv_check_device_error", "pkv_append_slots",
-           "pkv_mixed_layout", "pkv_decode_split", "pkv_run_decode_static", "pkv_context_only_views",
+           "pkv_mixed_layout", "pkv_decode_split", "pkv_decode_head_rows", "pkv_run_decode_static", "pkv_context_only_views",
            "pkv_plan_dense", "pkv_run_dense", "pkv_gather_kv", "pkv_run_decode_append", "pkv_selftest_wait_timeout"]
 
 
@@ -70,6 +70,7 @@ def load(path: str = LIB_PATH):
         "pkv_append_slots": ([i, i32p, i32p, i32p, i32p, i, i32p, i32p], i),
         "pkv_mixed_layout": ([i32p, i32p, i32p, i32p, i, i, i] + [i32p] * 9 + [ctypes.POINTER(i)], i),
         "pkv_decode_split": ([vp, i32p, i32p, i, i, i32p, ctypes.POINTER(i), ctypes.POINTER(i)], i),
+        "pkv_decode_head_rows": ([vp, i32p, i32p, i32p, i, i, i32p, ctypes.POINTER(i)], i),
         "pkv_run_decode_static": ([vp, vp, vp, vp, vp, i32p, i32p, i32p, i, i, ctypes.c_float, vp], i),
         "pkv_context_only_views": ([i, i32p, i32p, i32p, i32p, i, i32p, i32p, i32p, ctypes.POINTER(i)], i),
         "pkv_plan_dense": ([vp, i32p, i32p, i, i, i, ctypes.c_float, vp, ctypes.c_size_t, vp], i),
@@ -215,12 +216,23 @@ class Handle:
     def decode_split(self, kv_indptr, last_page_len, window_left=-1):
         kvp, lpl = _i32(kv_indptr), _i32(last_page_len)
         batch = len(kvp) - 1
-        cap = batch + 4 * max(1, self.cfg.sm_count or 256) + 8
+        cap = batch + 16 * max(1, self.cfg.sm_count or 256) + 8  # up to 8 decode CTAs per SM
         tiles = np.zeros(5 * cap, np.int32)
         nt, nc = ctypes.c_int(cap), ctypes.c_int()
         self._check(self.lib.pkv_decode_split(self.h, _p(kvp), _p(lpl), batch, int(window_left), _p(tiles),
                                               ctypes.byref(nt), ctypes.byref(nc)))
         return tiles[: 5 * nt.value].reshape(-1, 5), nc.value
+
+    def decode_head_rows(self, kv_indptr, kv_indices, last_page_len, window_left=-1):
+        """Cache rows of each decode CTA's first 4 chunks ([CTAs, 4], -1 past its end)."""
+        kvp, kvi, lpl = _i32(kv_indptr), _i32(kv_indices), _i32(last_page_len)
+        batch = len(kvp) - 1
+        cap = batch + 16 * max(1, self.cfg.sm_count or 256) + 8  # up to 8 decode CTAs per SM
+        rows = np.zeros(4 * cap, np.int32)
+        nc = ctypes.c_int(cap)
+        self._check(self.lib.pkv_decode_head_rows(self.h, _p(kvp), _p(kvi), _p(lpl), batch, int(window_left),
+                                                  _p(rows), ctypes.byref(nc)))
+        return rows[: 4 * nc.value].reshape(-1, 4)
 
 
 def append_slots(page_size, qo_indptr, kv_indptr, kv_indices, last_page_len):

@@ -40,6 +40,7 @@ struct DecodeArgs {
     float *lse;
     const DecodeTile *tiles;
     const int32_t *cta_ptr;
+    const int32_t *cta_rows;  // [CTA][kDecodeHeadChunks]: cache rows of its first chunks, -1 past its end
     const int32_t *pages;
     float *part_o;
     float *part_lse;
@@ -67,6 +68,26 @@ struct DecodeArgs {
 
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kDecodeMaxStages = 16;
+static_assert(kDecodeHeadChunks == 4, "a CTA's head rows are read as one int4");
+
+// C consecutive fp32 columns of a partial (C = 2, 4 or 8; 8- or 16-byte aligned), read at L2.
+template <int C>
+__device__ __forceinline__ void load_cols(float (&x)[C], const float *src) {
+    if constexpr (C == 2) {
+        const float2 t = __ldcg(reinterpret_cast<const float2 *>(src));
+        x[0] = t.x;
+        x[1] = t.y;
+    } else {
+#pragma unroll
+        for (int i = 0; i < C / 4; ++i) {
+            const float4 t = __ldcg(reinterpret_cast<const float4 *>(src) + i);
+            x[4 * i] = t.x;
+            x[4 * i + 1] = t.y;
+            x[4 * i + 2] = t.z;
+            x[4 * i + 3] = t.w;
+        }
+    }
+}
 
 // Merge the split-KV partials of cut row `m` (at most kFusedMergeMaxPieces of them) for
 // the g heads of kv head `hk`, one warp: with w_j = exp(lse_j - max lse),
@@ -107,20 +128,6 @@ __device__ __forceinline__ void merge_row_heads(const struct DecodeArgs &a, int 
     }
 }
 
-// The 16-key chunks of a tile: keys [base + 16 k, base + 16 k + 16) for k in [k0, nk),
-// of which positions below `end` belong to the tile (its last page may be cut short by
-// the row's end).
-struct ChunkRange {
-    int base, end, k0, nk;
-};
-__device__ __forceinline__ ChunkRange chunk_range(const DecodeTile &t, int P) {
-    ChunkRange c;
-    c.base = t.page_begin * P;
-    c.end = min(t.length, (t.page_begin + t.page_count) * P);
-    c.k0 = (max(t.lo, c.base) - c.base) / kDecodeKeysPerStage;
-    c.nk = (c.end - c.base + kDecodeKeysPerStage - 1) / kDecodeKeysPerStage;
-    return c;
-}
 
 // Byte offset, inside one 64-column half of a stage, of key `tok` (0..15) of local head
 // `hk`, and its 128-byte swizzle phase (`vrow`: a row offset inside the box, 0 here).
@@ -155,6 +162,15 @@ __global__ void __launch_bounds__((D > 128 ? 4 + (SMALL ? 2 : 1) : 8 + (SMALL ? 
     const int P = a.page_size;
     const int t_begin = a.cta_ptr[blockIdx.x];
     const int t_end = a.cta_ptr[blockIdx.x + 1];
+    // The plan's arrays come from the host's copy, never from a kernel, so they are read before
+    // waiting for the previous kernel: the TMA producer's first chunks need only their cache
+    // rows, which the planner stored beside the CTA's tile range (no dependent tile and
+    // page-id loads before the first copies), and its first tile is loaded meanwhile.
+    // Inputs, the cache and the merge counters may come from the previous kernel and are read
+    // only after the wait.
+    int4 head_rows = make_int4(-1, -1, -1, -1);
+    if (!SMALL && warp == Hc && lane == 0)
+        head_rows = reinterpret_cast<const int4 *>(a.cta_rows)[blockIdx.x];
     if (t_begin >= t_end) return;  // an idle CTA of a launch at the handle's maxima
     int *err = &a.hdr->err;
     const float scale_log2 = a.hdr->scale_log2;
@@ -174,20 +190,8 @@ __global__ void __launch_bounds__((D > 128 ? 4 + (SMALL ? 2 : 1) : 8 + (SMALL ? 
         prefetch_tmap(&tmap);
     }
     __syncthreads();
-    // The plan's arrays come from the host's copy, never from a kernel: the TMA producer reads its
-    // first tile and page id before waiting for the previous kernel, so those dependent loads
-    // overlap that kernel's tail.  Inputs, the cache and the merge counters may come from the
-    // previous kernel and are read only after the wait.
     DecodeTile first_tile{};
-    int first_row = -1;
-    if (!SMALL && warp == Hc && lane == 0) {
-        first_tile = a.tiles[t_begin];
-        const ChunkRange cr = chunk_range(first_tile, P);
-        if (cr.k0 < cr.nk) {
-            const int pos0 = cr.base + cr.k0 * kDecodeKeysPerStage;
-            first_row = a.pages[first_tile.kv_base + (pos0 >> a.page_shift)] * 2 * P + (pos0 & (P - 1));
-        }
-    }
+    if (!SMALL && warp == Hc && lane == 0) first_tile = a.tiles[t_begin];
     griddep_wait();
     griddep_launch();
 
@@ -262,12 +266,28 @@ __global__ void __launch_bounds__((D > 128 ? 4 + (SMALL ? 2 : 1) : 8 + (SMALL ? 
             const uint32_t box_bytes = (uint32_t)a.box_rows * Hc * 128;
             uint32_t it = 0;
             if (!SMALL) {
-                // one box (of K and of V) per chunk: its page id is loaded after the slot frees
+                // the first chunks into the empty stages, from the planner's rows
+                const int hr[kDecodeHeadChunks] = {head_rows.x, head_rows.y, head_rows.z, head_rows.w};
+                int nhead = 0;
+#pragma unroll
+                for (int i = 0; i < kDecodeHeadChunks; ++i)
+                    if (nhead == i && i < a.stages && hr[i] >= 0) {
+                        uint8_t *st = smem + (size_t)i * a.stage_bytes;
+                        mbar_arrive_expect_tx(&full[i], (uint32_t)(nkv * HALVES) * box_bytes);
+                        for (int kv = 0; kv < nkv; ++kv)
+#pragma unroll
+                            for (int h = 0; h < HALVES; ++h)
+                                tma_load_3d(st + (kv * HALVES + h) * half_stride, &tmap, &full[i], h * 64,
+                                            hr[i] + kv * P, hg * Hc);
+                        nhead = i + 1;
+                    }
+                // then one box (of K and of V) per chunk: its page id is loaded after the slot frees
                 for (int ti = t_begin; ti < t_end; ++ti) {
                     const DecodeTile t = ti == t_begin ? first_tile : a.tiles[ti];
                     const ChunkRange cr = chunk_range(t, P);
                     bool ok = true;
                     for (int k = cr.k0; k < cr.nk; ++k, ++it) {
+                        if (it < (uint32_t)nhead) continue;  // issued above
                         const int s = it % a.stages;
                         const uint32_t use = it / a.stages;
                         if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, err, kErrWaitEmpty)) {
@@ -275,9 +295,7 @@ __global__ void __launch_bounds__((D > 128 ? 4 + (SMALL ? 2 : 1) : 8 + (SMALL ? 
                             break;
                         }
                         const int pos0 = cr.base + k * kDecodeKeysPerStage;
-                        const int row = ti == t_begin && k == cr.k0
-                                            ? first_row
-                                            : a.pages[t.kv_base + (pos0 >> a.page_shift)] * 2 * P + (pos0 & (P - 1));
+                        const int row = a.pages[t.kv_base + (pos0 >> a.page_shift)] * 2 * P + (pos0 & (P - 1));
                         uint8_t *st = smem + (size_t)s * a.stage_bytes;
                         mbar_arrive_expect_tx(&full[s], (uint32_t)(nkv * HALVES) * box_bytes);
                         for (int kv = 0; kv < nkv; ++kv)
@@ -555,90 +573,86 @@ __global__ void __launch_bounds__((D > 128 ? 4 + (SMALL ? 2 : 1) : 8 + (SMALL ? 
 
 // Merge the split-KV partials of each cut row when the plan does not fuse merges into the
 // decode kernel: with w_j = exp(lse_j - max lse), o = sum_j w_j o_j / sum_j w_j and
-// lse = max lse + ln sum_j w_j.  One CTA per (cut row, q head), 256 threads: one warp
-// reduces the row's lse values to the max and the weight sum; then thread (slot, c) sums
-// pieces slot, slot + S, ... (S = 256 / (D/4) slots) for 4 columns c, so every partial of
-// the row is in flight at once, and the slots are added through shared memory.
-constexpr int kMergeThreads = 256;
+// lse = max lse + ln sum_j w_j.  One warp per (cut row, q head), eight to a CTA: lane j
+// holds piece j's lse, and every lane requests its D/32 columns of the row's first B pieces
+// together with the lse values, before the weights are known, so that a row of up to B pieces
+// costs one round trip to L2 after its MergeRow; longer rows take one more per B pieces (each
+// batch's loads issued together).  B pieces hold B * D/32 registers: the small instance
+// (64) keeps enough warps resident for the many rows of a batch, the large one (128) takes
+// the rows of many pieces of long contexts in one batch.
+constexpr int kMergeWarps = 8;
+constexpr int merge_batch(int D, bool large) {
+    return (large ? 128 : 64) / (D / 32) < 32 ? (large ? 128 : 64) / (D / 32) : 32;
+}
 
-// Pieces of a row whose weights warp 0 keeps in shared memory and whose partial columns the
-// threads request before those weights are known; rows with more pieces take a second loop.
-constexpr int kMergeFastPieces = 32;
-
-template <int D>
-__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const PlanHeader *hdr, const MergeRow *rows,
-                                                              const float *part_o, const float *part_lse,
-                                                              __nv_bfloat16 *out, float *lse, int Hq) {
-    constexpr int PER = D / 4;                      // threads per piece row (4 columns each)
-    constexpr int SLOTS = kMergeThreads / PER;      // pieces the CTA reads side by side
-    constexpr int NPER = kMergeFastPieces / SLOTS;  // pieces per thread requested up front
-    __shared__ float4 s_acc[kMergeThreads];
-    __shared__ float s_w[kMergeFastPieces];
-    __shared__ float s_red[2];
+template <int D, int B>
+__global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const PlanHeader *hdr, const MergeRow *rows,
+                                                                 const float *part_o, const float *part_lse,
+                                                                 __nv_bfloat16 *out, float *lse, int Hq) {
+    constexpr int C = D / 32;  // columns per lane: 2, 4 or 8
+    static_assert(B >= 1 && B <= 32, "a batch's weights come from one lane each");
+    const int lane = threadIdx.x & 31;
+    const long long u = (long long)blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
+    const int m = (int)(u / Hq), h = (int)(u % Hq);
     // the plan's own values (copied before the decode launch) are read before waiting for the
     // decode kernel; the partials it writes only after
-    const bool active = !hdr->fused_merge && (int)blockIdx.x < hdr->num_merge;
+    const bool active = !hdr->fused_merge && m < hdr->num_merge;
     MergeRow mr{};
-    if (active) mr = rows[blockIdx.x];
+    if (active) mr = rows[m];
     griddep_wait();
     griddep_launch();
     if (!active || mr.out_token < 0) return;
-    const int h = blockIdx.y;
     const int count = mr.count;
-    const float *lse_of = part_lse + (size_t)mr.first * Hq + h;  // piece j at lse_of[j * Hq]
-    const int slot = threadIdx.x / PER, c = (threadIdx.x % PER) * 4;
-    auto piece_o = [&](int j) {
-        return __ldcg(reinterpret_cast<const float4 *>(part_o + ((size_t)(mr.first + j) * Hq + h) * D + c));
-    };
-    // this thread's first pieces' partial columns: requested before the weights are known
-    float4 v[NPER];
+    const float *lse_of = part_lse + (size_t)mr.first * Hq + h;              // piece j at lse_of[j * Hq]
+    const float *o_of = part_o + ((size_t)mr.first * Hq + h) * D + lane * C;  // piece j at o_of[j * Hq * D]
+    auto load = [&](float (&dst)[C], int j) { load_cols<C>(dst, o_of + (size_t)j * Hq * D); };
+    const float lj = lane < count ? __ldcg(lse_of + (size_t)lane * Hq) : -INFINITY;
+    float x[B][C];
 #pragma unroll
-    for (int k = 0; k < NPER; ++k) {
-        const int j = slot + k * SLOTS;
-        v[k] = j < count ? piece_o(j) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    // warp 0: M = max_j lse_j, w_j = exp(lse_j - M) (the first pieces' into shared memory), sum w_j
-    if (threadIdx.x < 32) {
-        float M = -INFINITY;
-        for (int j = threadIdx.x; j < count; j += 32) M = fmaxf(M, __ldcg(lse_of + (size_t)j * Hq));
+    for (int j = 0; j < B; ++j)
+        if (j < count) load(x[j], j);
+    // M = max_j lse_j and sum_j w_j over the warp (pieces past 32: one more lse each per lane)
+    float M = lj;
+    for (int j = lane + 32; j < count; j += 32) M = fmaxf(M, __ldcg(lse_of + (size_t)j * Hq));
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-        float sum = 0.f;
-        for (int j = threadIdx.x; j < count; j += 32) {
-            const float w = __expf(__ldcg(lse_of + (size_t)j * Hq) - M);
-            if (j < kMergeFastPieces) s_w[j] = w;
-            sum += w;
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    const float wl = lane < count ? __expf(lj - M) : 0.f;
+    float sum = wl;
+    for (int j = lane + 32; j < count; j += 32) sum += __expf(__ldcg(lse_of + (size_t)j * Hq) - M);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    float acc[C];
+#pragma unroll
+    for (int c = 0; c < C; ++c) acc[c] = 0.f;
+    for (int j0 = 0;;) {
+#pragma unroll
+        for (int j = 0; j < B; ++j) {
+            const float w0 = __shfl_sync(0xffffffffu, wl, (j0 + j) & 31);
+            if (j0 + j < count) {
+                const float w = j0 + j < 32 ? w0 : __expf(__ldcg(lse_of + (size_t)(j0 + j) * Hq) - M);
+#pragma unroll
+                for (int c = 0; c < C; ++c) acc[c] += w * x[j][c];
+            }
         }
+        j0 += B;
+        if (j0 >= count) break;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-        if (threadIdx.x == 0) {
-            s_red[0] = M;
-            s_red[1] = sum;
-        }
+        for (int j = 0; j < B; ++j)  // the next batch (rows of many pieces)
+            if (j0 + j < count) load(x[j], j0 + j);
     }
-    __syncthreads();
-    const float M = s_red[0];
-    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    auto add = [&](float w, const float4 &x) {
-        o.x += w * x.x;
-        o.y += w * x.y;
-        o.z += w * x.z;
-        o.w += w * x.w;
-    };
+    const float inv = 1.f / sum;
+    uint32_t packed[C / 2];
 #pragma unroll
-    for (int k = 0; k < NPER; ++k)
-        if (slot + k * SLOTS < count) add(s_w[slot + k * SLOTS], v[k]);
-    for (int j = slot + NPER * SLOTS; j < count; j += SLOTS)  // rows of many pieces
-        add(__expf(__ldcg(lse_of + (size_t)j * Hq) - M), piece_o(j));
-    s_acc[threadIdx.x] = o;
-    __syncthreads();
-    if (slot == 0) {
-        for (int k = 1; k < SLOTS; ++k) add(1.f, s_acc[k * PER + threadIdx.x]);
-        const float inv = 1.f / s_red[1];
-        __nv_bfloat16 *dst = out + ((size_t)mr.out_token * Hq + h) * D + c;
-        *reinterpret_cast<uint2 *>(dst) = make_uint2(pack_bf16(o.x * inv, o.y * inv), pack_bf16(o.z * inv, o.w * inv));
-        if (lse && c == 0) lse[(size_t)mr.out_token * Hq + h] = M + __logf(s_red[1]);
+    for (int c = 0; c < C; c += 2) packed[c / 2] = pack_bf16(acc[c] * inv, acc[c + 1] * inv);
+    __nv_bfloat16 *dst = out + ((size_t)mr.out_token * Hq + h) * D + lane * C;
+    if constexpr (C == 2) {
+        *reinterpret_cast<uint32_t *>(dst) = packed[0];
+    } else if constexpr (C == 4) {
+        *reinterpret_cast<uint2 *>(dst) = make_uint2(packed[0], packed[1]);
+    } else {
+        *reinterpret_cast<uint4 *>(dst) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
     }
+    if (lse && lane == 0) lse[(size_t)mr.out_token * Hq + h] = M + __logf(sum);
 }
 
 
@@ -808,6 +822,7 @@ cudaError_t launch_decode(const Shape &s, const Plan &p, const CUtensorMap &tm, 
     a.lse = lse;
     a.tiles = reinterpret_cast<const DecodeTile *>(w + p.lay.dec_tiles);
     a.cta_ptr = reinterpret_cast<const int32_t *>(w + p.lay.dec_cta_ptr);
+    a.cta_rows = reinterpret_cast<const int32_t *>(w + p.lay.dec_cta_rows);
     a.pages = reinterpret_cast<const int32_t *>(w + p.lay.dec_pages);
     a.part_o = reinterpret_cast<float *>(w + p.lay.part_o);
     a.part_lse = reinterpret_cast<float *>(w + p.lay.part_lse);
@@ -846,9 +861,18 @@ cudaError_t launch_decode(const Shape &s, const Plan &p, const CUtensorMap &tm, 
     // and it returns at once when the plan merged inside the decode kernel)
     const int merges = s.graph_static ? sc.num_merge : (p.fused_merge ? 0 : p.num_merge);
     if (merges) {
-        const dim3 mgrid(merges, s.num_qo_heads);
-        auto mk = s.head_dim == 64 ? dev::merge_kernel<64> : s.head_dim == 128 ? dev::merge_kernel<128> : dev::merge_kernel<256>;
-        e = launch_pdl(mk, mgrid, dim3(dev::kMergeThreads), 0, st, static_cast<const PlanHeader *>(a.hdr),
+        const long long warps = (long long)merges * s.num_qo_heads;
+        const dim3 mgrid((unsigned)((warps + dev::kMergeWarps - 1) / dev::kMergeWarps));
+        // the large batch for rows of more pieces than the small one holds (graph mode, whose
+        // launch serves every later plan, keeps the small one)
+        const bool large = !s.graph_static && p.max_pieces > dev::merge_batch(s.head_dim, false);
+        using dev::merge_batch;
+        auto mk = s.head_dim == 64    ? dev::merge_kernel<64, merge_batch(64, false)>
+                  : s.head_dim == 128 ? (large ? dev::merge_kernel<128, merge_batch(128, true)>
+                                               : dev::merge_kernel<128, merge_batch(128, false)>)
+                                      : (large ? dev::merge_kernel<256, merge_batch(256, true)>
+                                               : dev::merge_kernel<256, merge_batch(256, false)>);
+        e = launch_pdl(mk, mgrid, dim3(dev::kMergeWarps * 32), 0, st, static_cast<const PlanHeader *>(a.hdr),
                        reinterpret_cast<const MergeRow *>(w + p.lay.merge_rows), static_cast<const float *>(a.part_o),
                        static_cast<const float *>(a.part_lse), a.out, lse, s.num_qo_heads);
     }

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <nvtx3/nvToolsExt.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -512,6 +513,29 @@ extern "C" pkv_status pkv_decode_split(pkv_handle_t h, const int32_t *kvp, const
     }
     *num_tiles = (int)dt.size();
     *num_ctas = dt.empty() ? 0 : (int)cta.size() - 1;
+    return PKV_OK;
+}
+
+extern "C" pkv_status pkv_decode_head_rows(pkv_handle_t h, const int32_t *kvp, const int32_t *kvi, const int32_t *lpl,
+                                           int batch, int window_left, int32_t *rows, int *num_ctas) {
+    NvtxCall nvtx_range(h, "pkv_decode_head_rows");
+    if (!h || !kvp || !kvi || !lpl || !rows || !num_ctas || batch < 0) return PKV_ERR_INVALID;
+    std::string err;
+    const int rc = pkv::validate_rows(h->shape, PKV_MODE_DECODE, nullptr, kvp, kvi, lpl, batch, window_left, err);
+    if (rc) return fail(h, (pkv_status)rc, err);
+    std::vector<int32_t> qt(batch), ot(batch);
+    for (int r = 0; r < batch; ++r) qt[r] = ot[r] = r;
+    std::vector<pkv::DecodeTile> dt;
+    std::vector<int32_t> cta;
+    std::vector<pkv::MergeRow> mg;
+    int parts = 0;
+    pkv::decode_split(h->shape, batch, kvp, lpl, qt.data(), ot.data(), window_left, dt, cta, mg, parts);
+    const int ctas = dt.empty() ? 0 : (int)cta.size() - 1;
+    if (ctas > *num_ctas) return fail(h, PKV_ERR_INVALID, "row buffer too small");
+    const std::vector<int32_t> pages(kvi, kvi + kvp[batch]);
+    const std::vector<int32_t> hr = pkv::decode_head_rows(h->shape, dt, cta, pages);
+    std::copy(hr.begin(), hr.end(), rows);
+    *num_ctas = ctas;
     return PKV_OK;
 }
 

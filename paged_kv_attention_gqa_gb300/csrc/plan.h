@@ -63,6 +63,33 @@ struct DecodeTile {
 };
 static_assert(sizeof(DecodeTile) == 48, "DecodeTile is 12 ints");
 
+#if defined(__CUDACC__)
+#define PKV_HOST_DEVICE __host__ __device__ __forceinline__
+#else
+#define PKV_HOST_DEVICE inline
+#endif
+
+// The 16-key chunks of a tile: keys [base + 16 k, base + 16 k + 16) for k in [k0, nk),
+// of which positions below `end` belong to the tile (its last page may be cut short by
+// the row's end).  The host planner and the decode kernel walk the same chunks.
+struct ChunkRange {
+    int base, end, k0, nk;
+};
+PKV_HOST_DEVICE ChunkRange chunk_range(const DecodeTile &t, int P) {
+    ChunkRange c;
+    c.base = t.page_begin * P;
+    const int stop = (t.page_begin + t.page_count) * P;
+    c.end = t.length < stop ? t.length : stop;
+    c.k0 = ((t.lo > c.base ? t.lo : c.base) - c.base) / kDecodeKeysPerStage;
+    c.nk = (c.end - c.base + kDecodeKeysPerStage - 1) / kDecodeKeysPerStage;
+    return c;
+}
+
+// Chunks of each decode CTA whose cache rows (page id * 2 * page_size + slot) the planner
+// stores beside its tile range: the TMA producer issues them as soon as the previous kernel
+// allows, without first loading the CTA's tile and then its page id.
+constexpr int kDecodeHeadChunks = 4;
+
 // A row whose visible pages were split over several CTAs: its partials
 // [first, first + count) are merged into out_token by the CTA that finishes the last
 // piece (arrived counts finished pieces; the merging CTA sets it back to 0).
@@ -95,6 +122,7 @@ struct PlanLayout {
     size_t pf_pages = 0;       // int32[pf_nnz]:  page ids the prefill pass reads
     size_t dec_tiles = 0;      // DecodeTile[dec_tiles]
     size_t dec_cta_ptr = 0;    // int32[dec_ctas + 1]: tile range of each decode CTA
+    size_t dec_cta_rows = 0;   // int32[dec_ctas][kDecodeHeadChunks]: rows of each CTA's first chunks, -1 past its end
     size_t merge_rows = 0;     // MergeRow[num_merge]
     size_t pf_tiles = 0;       // PrefillTile[pf_tiles]
     size_t int_bytes = 0;      // end of the integer part (what the H2D copies)
@@ -193,6 +221,7 @@ struct Plan {
     int pf_nnz = 0;
     int dec_ctas = 0, dec_tiles = 0, num_partials = 0, num_merge = 0;
     int fused_merge = 0;         // every cut row has few pieces: merged inside the decode kernel
+    int max_pieces = 0;          // pieces of the most-cut row
     int pf_tiles = 0;
     PlanLayout lay;
     std::vector<uint8_t> image;
@@ -216,6 +245,10 @@ struct MixedLayout {
 int mixed_layout(const int32_t *qo, const int32_t *kvp, const int32_t *kvi, const int32_t *lpl, int batch,
                  int max_prefill_rows, int sink_page, MixedLayout &out, std::string &err);
 // Split the visible pages of a decode pass into per-CTA tiles.
+// Rows of each decode CTA's first kDecodeHeadChunks chunks (its tiles' chunks in the order the
+// kernel walks them), -1 past the CTA's last chunk: int32[ctas][kDecodeHeadChunks].
+std::vector<int32_t> decode_head_rows(const Shape &s, const std::vector<DecodeTile> &tiles,
+                                      const std::vector<int32_t> &cta_ptr, const std::vector<int32_t> &pages);
 void decode_split(const Shape &s, int rows, const int32_t *kvp, const int32_t *lpl, const int32_t *q_token,
                   const int32_t *out_token, int window_left, std::vector<DecodeTile> &tiles,
                   std::vector<int32_t> &cta_ptr, std::vector<MergeRow> &merges, int &num_partials,

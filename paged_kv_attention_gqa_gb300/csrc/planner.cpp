@@ -400,6 +400,8 @@ static PlanLayout layout_for(const Shape &s, int num_append, int dec_nnz, int pf
     at = align_up(at + sizeof(DecodeTile) * (size_t)dec_tiles);
     L.dec_cta_ptr = at;
     at = align_up(at + sizeof(int32_t) * (size_t)(dec_ctas + 1));
+    L.dec_cta_rows = at;
+    at = align_up(at + sizeof(int32_t) * kDecodeHeadChunks * (size_t)dec_ctas);
     L.merge_rows = at;
     at = align_up(at + sizeof(MergeRow) * (size_t)num_merge);
     L.pf_tiles = at;
@@ -442,6 +444,25 @@ size_t workspace_bound(const Shape &s, int mode) {
         .total;
 }
 
+std::vector<int32_t> decode_head_rows(const Shape &s, const std::vector<DecodeTile> &tiles,
+                                      const std::vector<int32_t> &cta_ptr, const std::vector<int32_t> &pages) {
+    const int P = s.page_size;
+    const int ctas = cta_ptr.empty() ? 0 : (int)cta_ptr.size() - 1;
+    std::vector<int32_t> rows((size_t)ctas * kDecodeHeadChunks, -1);
+    for (int c = 0; c < ctas; ++c) {
+        int n = 0;
+        for (int ti = cta_ptr[c]; ti < cta_ptr[c + 1] && n < kDecodeHeadChunks; ++ti) {
+            const DecodeTile &t = tiles[ti];
+            const ChunkRange cr = chunk_range(t, P);
+            for (int k = cr.k0; k < cr.nk && n < kDecodeHeadChunks; ++k) {
+                const int pos0 = cr.base + k * kDecodeKeysPerStage;
+                rows[(size_t)c * kDecodeHeadChunks + n++] = pages[t.kv_base + (pos0 / P)] * 2 * P + pos0 % P;
+            }
+        }
+    }
+    return rows;
+}
+
 template <class T>
 static void put(std::vector<uint8_t> &img, size_t off, const T *src, size_t n) {
     if (n) std::memcpy(img.data() + off, src, n * sizeof(T));
@@ -460,8 +481,10 @@ static void finish_plan(const Shape &s, Plan &plan, int T, int window_left, cons
     plan.num_merge = (int)merges.size();
     plan.num_partials = partials;
     plan.fused_merge = 1;
-    for (const MergeRow &m : merges)
+    for (const MergeRow &m : merges) {
         if (m.count > kFusedMergeMaxPieces) plan.fused_merge = 0;
+        plan.max_pieces = std::max(plan.max_pieces, (int)m.count);
+    }
     plan.pf_tiles = (int)ptiles.size();
     if (s.graph_static) {
         // fixed layout at the maxima: captured launches keep pointing at the right arrays;
@@ -494,7 +517,11 @@ static void finish_plan(const Shape &s, Plan &plan, int T, int window_left, cons
     put(plan.image, plan.lay.dec_pages, dec_pages.data(), dec_pages.size());
     put(plan.image, plan.lay.pf_pages, pf_pages.data(), pf_pages.size());
     put(plan.image, plan.lay.dec_tiles, dtiles.data(), dtiles.size());
-    if (!cta_ptr.empty() && (plan.dec_ctas || s.graph_static)) put(plan.image, plan.lay.dec_cta_ptr, cta_ptr.data(), cta_ptr.size());
+    if (!cta_ptr.empty() && (plan.dec_ctas || s.graph_static)) {
+        put(plan.image, plan.lay.dec_cta_ptr, cta_ptr.data(), cta_ptr.size());
+        const std::vector<int32_t> rows = decode_head_rows(s, dtiles, cta_ptr, dec_pages);
+        put(plan.image, plan.lay.dec_cta_rows, rows.data(), rows.size());
+    }
     put(plan.image, plan.lay.merge_rows, merges.data(), merges.size());
     put(plan.image, plan.lay.pf_tiles, ptiles.data(), ptiles.size());
 }

@@ -152,6 +152,34 @@ def test_decode_split_covers_each_visible_page_once(lib, name, window, P, Hkv):
     assert sorted(parts.tolist()) == list(range(len(parts)))
 
 
+@pytest.mark.parametrize("name,window,P", [("batch", -1, 16), ("long", 4096, 16), ("tiny", -1, 16), ("tiny", 5, 16),
+                                           ("batch", -1, 64), ("long", 100, 64), ("long", 20, 32), ("batch", 0, 16)])
+@pytest.mark.parametrize("Hkv", [None, 1])
+def test_decode_head_rows_are_the_first_chunks_of_each_cta(lib, name, window, P, Hkv):
+    """The rows a decode CTA's first copies are issued from, written into the plan by the
+    planner, against the chunks rederived here from the split: CTA c's tiles in order, each
+    tile's 16-key chunks from the first one holding a visible key, the row of a chunk being
+    its first key's page id * 2P + slot; -1 past the CTA's last chunk."""
+    pb = _split_case(name, P)
+    Hkv = Hkv or pb.num_kv_heads
+    h = _handle(num_qo_heads=Hkv * pb.num_qo_heads // pb.num_kv_heads, num_kv_heads=Hkv, head_dim=pb.head_dim,
+                num_cache_pages=pb.max_pages, page_size=P)
+    tiles, ctas = h.decode_split(pb.kv_indptr, pb.last_page_len, window)
+    rows = h.decode_head_rows(pb.kv_indptr, pb.kv_indices, pb.last_page_len, window)
+    assert rows.shape == (ctas, 4)
+    want = [[] for _ in range(ctas)]
+    for r, page_begin, page_count, _, c in tiles.tolist():
+        L = int(pb.kv_lens[r])
+        lo = max(0, L - 1 - window) if window >= 0 else 0
+        base, end = page_begin * P, min(L, (page_begin + page_count) * P)
+        for pos0 in range(base + (max(lo, base) - base) // 16 * 16, end, 16):
+            want[c].append(int(pb.kv_indices[pb.kv_indptr[r] + pos0 // P]) * 2 * P + pos0 % P)
+    for c in range(ctas):
+        first = (want[c] + [-1] * 4)[:4]
+        assert rows[c].tolist() == first, c
+        assert want[c], c  # every CTA of a split has a chunk to read
+
+
 def test_nvtx_ranges_leave_host_results_unchanged(lib):
     """enable_nvtx (the wrappers' constructor flag) only opens a range per call: the split
     and a plan rejected before any copy come out the same, and a range opened by a call
