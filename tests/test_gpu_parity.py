@@ -71,6 +71,17 @@ def test_decode_forced_splits(sm_count):
     _check_step(pb, "decode", sm_count=sm_count, seed=3)
 
 
+@pytest.mark.parametrize("D,Hq,Hkv", [(64, 16, 4), (256, 16, 4)])
+@pytest.mark.parametrize("sm_count", [10, 40, 152, 300])
+def test_decode_merge_piece_counts(D, Hq, Hkv, sm_count):
+    """Rows cut into 3 to ~130 pieces at head_dim 64 and 256: the merge kernel's small and large
+    instances, one or several batches of pieces, and more than 32 pieces per row (lse values
+    past a lane each)."""
+    lens = [4000, 1200, 33, 1]
+    pb = wl.custom(6, lens, [1] * len(lens), num_qo_heads=Hq, num_kv_heads=Hkv, head_dim=D, page_size=16)
+    _check_step(pb, "decode", sm_count=sm_count, seed=4)
+
+
 # ------------------------------------------------------------------ append fused into the decode launch
 
 @pytest.mark.parametrize("D,Hq,Hkv", [(128, 32, 8), (64, 8, 2), (128, 16, 1)])
