@@ -56,7 +56,8 @@ def parse():
                     help="decode workloads: pkv_kv_append_planned + pkv_run_decode per layer instead of the fused call")
     ap.add_argument("--layers", type=int, default=0, help="fewer cache layers (profiling a small case)")
     ap.add_argument("--heads", default=None,
-                    help="Hq/Hkv/head_dim for --config prefill (the same lengths on another head shape, e.g. 16/8/256)")
+                    help="Hq/Hkv/head_dim for --config prefill or batch (the same lengths on another head shape, "
+                         "e.g. 16/8/256 or 8/1/128)")
     return ap.parse_args()
 
 
@@ -207,6 +208,10 @@ def prefill_flops(pb, causal=True, window_left=-1):
 def decode_workload(args):
     if args.config == "batch":
         pb = wl.config_batch_decode(seed=args.seed, num_layers=args.layers or 32)
+        if args.heads:
+            hq, hkv, d = (int(v) for v in args.heads.split("/"))
+            pb = wl.custom(args.seed, pb.kv_lens, pb.qo_lens, num_qo_heads=hq, num_kv_heads=hkv, head_dim=d,
+                           page_size=pb.page_size, num_layers=pb.num_layers, q_scale=pb.q_scale)
         window = -1
     elif args.config == "tiny":
         pb = wl.config_tiny(seed=args.seed)
@@ -287,7 +292,8 @@ def run_ours(args, rank, world):
     step_bytes = kv_layer_bytes * L
     value = world * step_bytes / (ms_step * 1e-3) / 1e9
     achieved = kv_layer_bytes / (launch_ms * 1e-3) / 1e9
-    traffic = kernel_traffic("decode.cu", "decode_batch128_traffic.md") if args.config == "batch" else None
+    traffic = (kernel_traffic("decode.cu", "decode_batch128_traffic.md") if args.config == "batch" and not args.heads
+               else None)
 
     # end to end through host buffers: per step the host index arrays (plan), and per
     # layer q / new K / new V in from pinned host memory, out + lse back to it

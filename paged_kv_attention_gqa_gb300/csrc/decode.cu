@@ -14,8 +14,9 @@
 //    V), so a CTA streams 16-key chunks of its heads: one producer thread issues TMA
 //    boxes (64-column halves, 128-byte swizzle) into a ring of stages, completion on an
 //    mbarrier; consumers release a stage through a second mbarrier.  A chunk is one box
-//    of K and one of V (page size >= 16) or two of each (8); pages below 8 slots are
-//    copied by the whole producer warp with 16-byte cp.async into the same layout.
+//    per 64-column half holding its K rows then its V rows (page size 16: a whole page),
+//    one box of K and one of V (page size > 16) or two of each (8); pages below 8 slots
+//    are copied by the whole producer warp with 16-byte cp.async into the same layout.
 //  * One consumer warp per kv head.  The g query heads of the group are the M dimension of
 //    a 16x8x16 bf16 tensor-core MMA (padded to 16 rows); keys are N for QK^T and K for PV.
 //    Online softmax in the exp2 domain with quad shuffles.
@@ -60,6 +61,7 @@ struct DecodeArgs {
     int box_rows;      // rows per head of one TMA box
     int kpb_shift;     // log2 of the keys one box holds per head
     int gather;        // 1: pages below 8 slots, copied by the producer warps (cp.async)
+    int kv_in_box;     // 1: one box holds a chunk's K rows, then its V rows (page size 16)
     int producers;     // producer warps (warps heads .. heads + producers - 1)
     int box_stride;    // bytes between boxes in a stage
     int stages;
@@ -130,7 +132,8 @@ __device__ __forceinline__ void merge_row_heads(const struct DecodeArgs &a, int 
 
 
 // Byte offset, inside one 64-column half of a stage, of key `tok` (0..15) of local head
-// `hk`, and its 128-byte swizzle phase (`vrow`: a row offset inside the box, 0 here).
+// `hk`, and its 128-byte swizzle phase (`vrow`: a row offset inside the box, 16 for V rows when a
+// box holds a chunk's K and V rows, else 0).
 struct RowAddr {
     uint32_t off;
     uint32_t phase;
@@ -179,7 +182,7 @@ __global__ void __launch_bounds__((D > 128 ? 4 + (SMALL ? 2 : 1) : 8 + (SMALL ? 
     const int kpb = 1 << a.kpb_shift;
     const int nb = kDecodeKeysPerStage / kpb;
     const uint32_t half_stride = (uint32_t)nb * a.box_stride;
-    const uint32_t v_region = HALVES * half_stride;
+    const uint32_t v_region = a.kv_in_box ? 0u : HALVES * half_stride;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < a.stages; ++s) {
@@ -262,7 +265,7 @@ __global__ void __launch_bounds__((D > 128 ? 4 + (SMALL ? 2 : 1) : 8 + (SMALL ? 
         if (warp > Hc) return;
         // ---------------- producer ----------------
         if (lane == 0) {
-            const int nkv = 2;
+            const int nkv = a.kv_in_box ? 1 : 2;  // boxes per 64-column half
             const uint32_t box_bytes = (uint32_t)a.box_rows * Hc * 128;
             uint32_t it = 0;
             if (!SMALL) {
@@ -365,7 +368,7 @@ __global__ void __launch_bounds__((D > 128 ? 4 + (SMALL ? 2 : 1) : 8 + (SMALL ? 
     const int k_chk = (lane >> 3) & 1;
     const int v_tok = (lane & 7) + (((lane >> 3) & 1) << 3);
     const int v_chk = lane >> 4;
-    const int vrow = 0;
+    const int vrow = a.kv_in_box ? kDecodeKeysPerStage : 0;  // V rows after K rows in one box
     const RowAddr ka = key_row(a, hk, k_tok, 0);
     RowAddr va = key_row(a, hk, v_tok, vrow);
     va.off += v_region;
@@ -840,6 +843,7 @@ cudaError_t launch_decode(const Shape &s, const Plan &p, const CUtensorMap &tm, 
     a.box_rows = s.dec_box_rows();
     a.kpb_shift = __builtin_ctz((unsigned)s.dec_keys_per_box());
     a.gather = s.dec_gather() ? 1 : 0;
+    a.kv_in_box = s.dec_kv_in_box() ? 1 : 0;
     a.producers = s.dec_producer_warps();
     a.box_stride = s.dec_box_stride();
     a.stages = decode_stages(s);

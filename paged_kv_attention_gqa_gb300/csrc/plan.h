@@ -177,13 +177,16 @@ struct Shape {
         return w < 1 ? 1 : (w > 4 ? 4 : w);
     }
     int dec_keys_per_box() const { return page_size == 8 ? 8 : 16; }
-    int dec_box_rows() const { return dec_keys_per_box(); }
+    // At page size 16 a chunk is one whole page, whose 16 K rows and 16 V rows are adjacent
+    // in the cache: one box of 32 rows takes both (K rows, then V rows), half the boxes.
+    bool dec_kv_in_box() const { return page_size == 16; }
+    int dec_box_rows() const { return dec_kv_in_box() ? 2 * dec_keys_per_box() : dec_keys_per_box(); }
     // Bytes between boxes in shared memory (a multiple of the 1024-byte swizzle atom).
     int dec_box_stride() const { return dec_box_rows() * dec_heads() * 128; }
     // One ring stage: the K and V boxes of a 16-key chunk, 64-column halves.
     uint32_t dec_stage_bytes() const {
         const uint32_t boxes = kDecodeKeysPerStage / dec_keys_per_box();
-        return 2u * (uint32_t)(head_dim / 64) * boxes * (uint32_t)dec_box_stride();
+        return (dec_kv_in_box() ? 1u : 2u) * (uint32_t)(head_dim / 64) * boxes * (uint32_t)dec_box_stride();
     }
     // Prefill: rows of one paged TMA box (one head); pages smaller than 8 slots are
     // gathered with 16-byte cp.async copies instead (a box would not fill a swizzle atom).
