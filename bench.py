@@ -239,11 +239,10 @@ def run_ours(args, rank, world):
     kvp, kvi, lpl = pb.kv_indptr, pb.kv_indices, pb.last_page_len
     h.plan(B.MODE_DECODE, None, kvp, kvi, lpl, workspace=ws, window_left=window)
     # launches per layer: the decode kernel (which also appends the layer's new tokens, or
-    # append + decode with --separate-append), + the merge kernel when some cut row has
-    # more pieces than the decode kernel merges itself (4)
+    # append + decode with --separate-append), + the merge kernel when some row is cut
     tiles, _ = h.decode_split(kvp, lpl, window)
-    pieces = np.bincount(tiles[tiles[:, 3] >= 0, 0]) if (tiles[:, 3] >= 0).any() else np.zeros(1, int)
-    launches_per_layer = (2 if args.separate_append else 1) + (1 if pieces.max() > 4 else 0)
+    cut = bool((tiles[:, 3] >= 0).any())
+    launches_per_layer = (2 if args.separate_append else 1) + (1 if cut else 0)
 
     ev_pairs = []
 
@@ -387,8 +386,10 @@ def run_ours(args, rank, world):
         "gpu_launches": int(args.steps * L * launches_per_layer),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
-                     "kernel": ("decode_kernel (one run_decode)" if args.separate_append else
-                                "decode_kernel (append and split-KV merge fused; one run_decode_append)"),
+                     "kernel": ("decode_kernel (+ merge_kernel when a row is cut; one run_decode)"
+                                if args.separate_append else
+                                "decode_kernel with the append fused (+ merge_kernel when a row is cut; one "
+                                "run_decode_append)"),
                      "launch_ms": round(launch_ms, 5), "peak_source": peaks["source"],
                      # launch_ms: one launch timed alone (events on both sides break the chain of
                      # programmatic launches); inside the step each launch's prologue overlaps the

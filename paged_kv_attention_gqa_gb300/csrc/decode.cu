@@ -45,7 +45,6 @@ struct DecodeArgs {
     const int32_t *pages;
     float *part_o;
     float *part_lse;
-    MergeRow *merges;
     PlanHeader *hdr;  // per-plan values (error word, sm_scale) in the workspace
     // fused append (null when the plan's tokens were appended by append_kernel): the new
     // tokens' K / V rows, the layer slice and each token's slot row in it
@@ -91,46 +90,6 @@ __device__ __forceinline__ void load_cols(float (&x)[C], const float *src) {
     }
 }
 
-// Merge the split-KV partials of cut row `m` (at most kFusedMergeMaxPieces of them) for
-// the g heads of kv head `hk`, one warp: with w_j = exp(lse_j - max lse),
-// o = sum_j w_j o_j / sum_j w_j and lse = max + ln sum_j w_j.  Lane j holds piece j's lse.
-template <int D, int G>
-__device__ __forceinline__ void merge_row_heads(const struct DecodeArgs &a, int m, int hk, int lane) {
-    constexpr int C = D / 32;  // columns per lane
-    const MergeRow mr = a.merges[m];
-    const int Hq = a.num_qo_heads;
-    for (int gi = 0; gi < G; ++gi) {
-        const int h = hk * G + gi;
-        const float lj = lane < mr.count ? __ldcg(a.part_lse + (size_t)(mr.first + lane) * Hq + h) : -INFINITY;
-        float M = lj;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-        const float wj = lane < mr.count ? __expf(lj - M) : 0.f;
-        float wsum = wj;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
-        float acc[C];
-#pragma unroll
-        for (int c = 0; c < C; ++c) acc[c] = 0.f;
-#pragma unroll
-        for (int j = 0; j < kFusedMergeMaxPieces; ++j) {
-            const float w = __shfl_sync(0xffffffffu, wj, j);
-            if (j < mr.count) {
-                const float *src = a.part_o + ((size_t)(mr.first + j) * Hq + h) * D + lane * C;
-#pragma unroll
-                for (int c = 0; c < C; ++c) acc[c] += w * __ldcg(src + c);
-            }
-        }
-        if (mr.out_token < 0) continue;
-        const float inv = 1.f / wsum;
-        __nv_bfloat16 *dst = a.out + ((size_t)mr.out_token * Hq + h) * D + lane * C;
-#pragma unroll
-        for (int c = 0; c < C; c += 2) *reinterpret_cast<uint32_t *>(dst + c) = pack_bf16(acc[c] * inv, acc[c + 1] * inv);
-        if (a.lse && lane == 0) a.lse[(size_t)mr.out_token * Hq + h] = M + __logf(wsum);
-    }
-}
-
-
 // Byte offset, inside one 64-column half of a stage, of key `tok` (0..15) of local head
 // `hk`, and its 128-byte swizzle phase (`vrow`: a row offset inside the box, 16 for V rows when a
 // box holds a chunk's K and V rows, else 0).
@@ -156,7 +115,6 @@ __global__ void __launch_bounds__((D > 128 ? 4 + (SMALL ? 2 : 1) : 8 + (SMALL ? 
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)a.stages * a.stage_bytes);
     uint64_t *empty = full + a.stages;
-    volatile int *last_piece = reinterpret_cast<volatile int *>(empty + a.stages);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -169,7 +127,7 @@ __global__ void __launch_bounds__((D > 128 ? 4 + (SMALL ? 2 : 1) : 8 + (SMALL ? 
     // waiting for the previous kernel: the TMA producer's first chunks need only their cache
     // rows, which the planner stored beside the CTA's tile range (no dependent tile and
     // page-id loads before the first copies), and its first tile is loaded meanwhile.
-    // Inputs, the cache and the merge counters may come from the previous kernel and are read
+    // Inputs and the cache may come from the previous kernel (an append, a merge) and are read
     // only after the wait.
     int4 head_rows = make_int4(-1, -1, -1, -1);
     if (!SMALL && warp == Hc && lane == 0)
@@ -177,7 +135,6 @@ __global__ void __launch_bounds__((D > 128 ? 4 + (SMALL ? 2 : 1) : 8 + (SMALL ? 
     if (t_begin >= t_end) return;  // an idle CTA of a launch at the handle's maxima
     int *err = &a.hdr->err;
     const float scale_log2 = a.hdr->scale_log2;
-    const bool fused_merge = a.hdr->fused_merge != 0;
     // stage layout: [K or V][64-column half][box]; with K and V in one box: [half][box]
     const int kpb = 1 << a.kpb_shift;
     const int nb = kDecodeKeysPerStage / kpb;
@@ -552,30 +509,12 @@ __global__ void __launch_bounds__((D > 128 ? 4 + (SMALL ? 2 : 1) : 8 + (SMALL ? 
                 if (gid < G) a.part_lse[(size_t)t.partial * Hq + h0] = lse0;
                 if (gid + 8 < G) a.part_lse[(size_t)t.partial * Hq + h1] = lse1;
             }
-            // The CTA that finishes the last piece of a cut row merges its partials (a
-            // counter per row; fences order the partials before the count and the merge's
-            // reads after it) -- when the plan keeps merges in this kernel.
-            // Every head group's CTA counts its piece; the last of all of them merges
-            // every kv head of the row.
-            if (!fused_merge) continue;
-            __threadfence();
-            named_barrier_sync(1, Hc * 32);
-            if (threadIdx.x == 0) {
-                MergeRow *mr = &a.merges[t.merge_row];
-                *last_piece = atomicAdd(&mr->arrived, 1) == mr->count * (int)gridDim.y - 1;
-            }
-            named_barrier_sync(1, Hc * 32);
-            if (*last_piece) {
-                __threadfence();
-                for (int h2 = hk; h2 < a.num_kv_heads; h2 += Hc) merge_row_heads<D, G>(a, t.merge_row, h2, lane);
-                if (threadIdx.x == 0) a.merges[t.merge_row].arrived = 0;  // ready for the next run
-            }
         }
     }
 }
 
-// Merge the split-KV partials of each cut row when the plan does not fuse merges into the
-// decode kernel: with w_j = exp(lse_j - max lse), o = sum_j w_j o_j / sum_j w_j and
+// Merge the split-KV partials of each cut row after the decode kernel: with
+// w_j = exp(lse_j - max lse), o = sum_j w_j o_j / sum_j w_j and
 // lse = max lse + ln sum_j w_j.  One warp per (cut row, q head), eight to a CTA: lane j
 // holds piece j's lse, and every lane requests its D/32 columns of the row's first B pieces
 // together with the lse values, before the weights are known, so that a row of up to B pieces
@@ -599,7 +538,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const PlanHeade
     const int m = (int)(u / Hq), h = (int)(u % Hq);
     // the plan's own values (copied before the decode launch) are read before waiting for the
     // decode kernel; the partials it writes only after
-    const bool active = !hdr->fused_merge && m < hdr->num_merge;
+    const bool active = m < hdr->num_merge;
     MergeRow mr{};
     if (active) mr = rows[m];
     griddep_wait();
@@ -829,7 +768,6 @@ cudaError_t launch_decode(const Shape &s, const Plan &p, const CUtensorMap &tm, 
     a.pages = reinterpret_cast<const int32_t *>(w + p.lay.dec_pages);
     a.part_o = reinterpret_cast<float *>(w + p.lay.part_o);
     a.part_lse = reinterpret_cast<float *>(w + p.lay.part_lse);
-    a.merges = reinterpret_cast<MergeRow *>(w + p.lay.merge_rows);
     a.hdr = reinterpret_cast<PlanHeader *>(w + p.lay.err);
     a.k_new = static_cast<const uint4 *>(k_new);
     a.v_new = static_cast<const uint4 *>(v_new);
@@ -861,9 +799,9 @@ cudaError_t launch_decode(const Shape &s, const Plan &p, const CUtensorMap &tm, 
     PKV_FOR_EACH_HEAD_DIM_AND_GROUP(PKV_DEC)
 #undef PKV_DEC
     if (e != cudaSuccess) return e;
-    // merges of rows cut into many pieces: a separate kernel (graph mode always launches it,
-    // and it returns at once when the plan merged inside the decode kernel)
-    const int merges = s.graph_static ? sc.num_merge : (p.fused_merge ? 0 : p.num_merge);
+    // the merge of the rows cut into several pieces (graph mode always launches it at the
+    // maxima; its warps past the plan's cut rows return at once)
+    const int merges = s.graph_static ? sc.num_merge : p.num_merge;
     if (merges) {
         const long long warps = (long long)merges * s.num_qo_heads;
         const dim3 mgrid((unsigned)((warps + dev::kMergeWarps - 1) / dev::kMergeWarps));

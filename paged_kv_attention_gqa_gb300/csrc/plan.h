@@ -25,10 +25,6 @@ constexpr int kPrefillKeysPerStage = 64;
 constexpr int kDecodeKeysPerStage = 16;
 // Shared memory per SM given to decode rings (split among the SM's decode CTAs).
 constexpr uint32_t kDecodeRingBytes = 200u * 1024u;
-// A cut decode row with at most this many pieces is merged inside the decode kernel by
-// the CTA that finishes its last piece; longer ones by the separate merge kernel, whose
-// CTAs spread one row's heads over many SMs.
-constexpr int kFusedMergeMaxPieces = 4;
 
 // First bytes of every plan in the workspace: the per-plan values the kernels read on
 // the device, so that launches captured into a CUDA graph stay valid for later plans
@@ -43,7 +39,6 @@ struct PlanHeader {
     int32_t window_left;
     float scale_log2;     // sm_scale * log2(e)
     int32_t dense;        // prefill tiles read contiguous K / V runs instead of pages
-    int32_t fused_merge;  // decode: the CTA finishing a cut row's last piece merges it
 };
 static_assert(sizeof(PlanHeader) <= kAlign, "the header fits its aligned slot");
 
@@ -91,13 +86,12 @@ PKV_HOST_DEVICE ChunkRange chunk_range(const DecodeTile &t, int P) {
 constexpr int kDecodeHeadChunks = 4;
 
 // A row whose visible pages were split over several CTAs: its partials
-// [first, first + count) are merged into out_token by the CTA that finishes the last
-// piece (arrived counts finished pieces; the merging CTA sets it back to 0).
+// [first, first + count) are merged into out_token by the merge kernel.
 struct MergeRow {
     int32_t out_token;
     int32_t first;
     int32_t count;
-    int32_t arrived;
+    int32_t pad;  // 16 bytes: one vector load
 };
 
 // One prefill work tile: up to BQ consecutive new tokens of one row, all q heads of one
@@ -223,7 +217,6 @@ struct Plan {
     int dec_nnz = 0;
     int pf_nnz = 0;
     int dec_ctas = 0, dec_tiles = 0, num_partials = 0, num_merge = 0;
-    int fused_merge = 0;         // every cut row has few pieces: merged inside the decode kernel
     int max_pieces = 0;          // pieces of the most-cut row
     int pf_tiles = 0;
     PlanLayout lay;

@@ -284,7 +284,7 @@ void decode_split(const Shape &s, int rows, const int32_t *kvp, const int32_t *l
         m.out_token = out_token[rr];
         m.first = num_partials;
         m.count = (int)row_tiles[rr].size();
-        m.arrived = 0;
+        m.pad = 0;
         for (int ti : row_tiles[rr]) {
             tiles[ti].partial = num_partials++;
             tiles[ti].merge_row = (int)merges.size();
@@ -480,11 +480,7 @@ static void finish_plan(const Shape &s, Plan &plan, int T, int window_left, cons
     plan.dec_ctas = dtiles.empty() ? 0 : (int)cta_ptr.size() - 1;
     plan.num_merge = (int)merges.size();
     plan.num_partials = partials;
-    plan.fused_merge = 1;
-    for (const MergeRow &m : merges) {
-        if (m.count > kFusedMergeMaxPieces) plan.fused_merge = 0;
-        plan.max_pieces = std::max(plan.max_pieces, (int)m.count);
-    }
+    for (const MergeRow &m : merges) plan.max_pieces = std::max(plan.max_pieces, (int)m.count);
     plan.pf_tiles = (int)ptiles.size();
     if (s.graph_static) {
         // fixed layout at the maxima: captured launches keep pointing at the right arrays;
@@ -511,7 +507,6 @@ static void finish_plan(const Shape &s, Plan &plan, int T, int window_left, cons
     hdr.window_left = window_left;
     hdr.scale_log2 = plan.sm_scale * 1.4426950408889634f;
     hdr.dense = mode == PKV_MODE_DENSE ? 1 : 0;
-    hdr.fused_merge = plan.fused_merge;
     put(plan.image, plan.lay.err, &hdr, 1);
     put(plan.image, plan.lay.append_rows, app.data(), app.size());
     put(plan.image, plan.lay.dec_pages, dec_pages.data(), dec_pages.size());

@@ -72,7 +72,7 @@ def test_decode_append_fused_page_sizes(P, Hq, Hkv, D, sm_count):
 @pytest.mark.parametrize("sm_count", [1, 3, 40])
 def test_decode_page_sizes_forced_splits(P, sm_count):
     """Pieces cut at page boundaries of every page size; 40 CTAs cut the 3000-key row into
-    more pieces than the in-kernel merge takes (separate merge kernel), 3 into fewer."""
+    many pieces for the merge kernel, 3 into few."""
     lens = [3000, 5, 64, 1, 333]
     pb = wl.custom(110 + P, lens, [1] * len(lens), num_qo_heads=32, num_kv_heads=8, head_dim=128, page_size=P)
     _check_step(pb, "decode", sm_count=sm_count, seed=P + 1)
@@ -222,9 +222,9 @@ def test_mixed_odd_groups(g):
 @pytest.mark.parametrize("Hq,Hkv,D", [(16, 16, 128), (32, 16, 128), (24, 12, 64), (40, 40, 128), (32, 16, 256)])
 @pytest.mark.parametrize("sm_count", [0, 10, 60])
 def test_decode_many_kv_heads(Hq, Hkv, D, sm_count):
-    """Several CTA head groups sharing the SMs; 10 SMs cut the long rows into few pieces
-    (merged inside the decode kernel by the last CTA of all head groups), 60 into more
-    than that merge takes (separate merge kernel)."""
+    """Several CTA head groups sharing the SMs, each group cutting the rows at its own piece
+    boundaries: 10 SMs cut the long rows into few pieces, 60 into many (the merge kernel
+    takes every head group's partials of a row)."""
     lens = [1, 17, 100, 1000, 2048]
     pb = wl.custom(200 + Hkv, lens, [1] * len(lens), num_qo_heads=Hq, num_kv_heads=Hkv, head_dim=D, page_size=16)
     _check_step(pb, "decode", sm_count=sm_count, seed=Hkv)
