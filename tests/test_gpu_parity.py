@@ -82,6 +82,24 @@ def test_decode_merge_piece_counts(D, Hq, Hkv, sm_count):
     _check_step(pb, "decode", sm_count=sm_count, seed=4)
 
 
+# (head_dim, Hq, Hkv, row length, SM count, pieces of the long row): each merge-kernel instance
+# at the end of its batch of pieces and one past it (B = 32 / 16 / 8 small, 32 / 32 / 16 large at
+# head_dim 64 / 128 / 256), and 32 / 33 pieces (the lse values past one per lane)
+MERGE_EDGES = [(64, 16, 4, 3000, 16, 32), (64, 16, 4, 4100, 17, 33), (128, 32, 8, 3000, 16, 16),
+               (128, 32, 8, 3500, 18, 17), (128, 32, 8, 3000, 32, 32), (128, 32, 8, 4100, 33, 33),
+               (256, 16, 4, 3000, 8, 8), (256, 16, 4, 3000, 9, 9), (256, 16, 4, 3000, 16, 16),
+               (256, 16, 4, 3500, 18, 17), (256, 16, 4, 4100, 33, 33)]
+
+
+@pytest.mark.parametrize("D,Hq,Hkv,L,sm_count,pieces", MERGE_EDGES)
+def test_decode_merge_batch_edges(D, Hq, Hkv, L, sm_count, pieces):
+    pb = wl.custom(8, [L, 40], [1, 1], num_qo_heads=Hq, num_kv_heads=Hkv, head_dim=D, page_size=16)
+    h = G.make_handle(pb, sm_count=sm_count)
+    tiles, _ = h.decode_split(pb.kv_indptr, pb.last_page_len)
+    assert np.bincount(tiles[:, 0]).max() == pieces, "the split no longer cuts the row into this many pieces"
+    _check_step(pb, "decode", sm_count=sm_count, seed=9)
+
+
 # ------------------------------------------------------------------ append fused into the decode launch
 
 @pytest.mark.parametrize("D,Hq,Hkv", [(128, 32, 8), (64, 8, 2), (128, 16, 1)])

@@ -180,6 +180,17 @@ def test_decode_head_rows_are_the_first_chunks_of_each_cta(lib, name, window, P,
         assert want[c], c  # every CTA of a split has a chunk to read
 
 
+def test_decode_head_rows_rejects_invalid_rows(lib):
+    """The head-row export validates its index arrays as pkv_plan does (it reads page ids)."""
+    h = _handle(num_cache_pages=64)
+    for kvp, kvi, lpl in (([0, 2, 1], [0, 1], [1, 1]),       # kv_indptr decreases
+                          ([0, 2], [0, 99], [1]),            # a page id past the cache
+                          ([0, 1], [0], [17])):              # last_page_len above the page size
+        with pytest.raises(B.PkvError) as e:
+            h.decode_head_rows(kvp, kvi, lpl)
+        assert e.value.status == B.ERR_INVALID
+
+
 def test_nvtx_ranges_leave_host_results_unchanged(lib):
     """enable_nvtx (the wrappers' constructor flag) only opens a range per call: the split
     and a plan rejected before any copy come out the same, and a range opened by a call
