@@ -7,8 +7,9 @@ library a workspace.  For them the library keeps the plan and the split-KV parti
 one decode in a fixed 16 MiB device array of its own.  These tests call that entry point
 through the C ABI twice in a row per case and check each result against the oracle and
 against the workspace-based pkv_run_decode, at the tolerances of the other parity tests:
-once with rows cut into many pieces (the separate merge kernel), once with every cut
-row in at most four pieces (the merge inside the decode kernel), once with a window.
+once with rows cut into many pieces (the large merge-kernel instance, several batches),
+once with every cut row in at most four pieces (one batch of the small instance), once
+with a window.
 The file is collected last, and its tests pass alone or after the others.
 """
 import ctypes
