@@ -22,6 +22,9 @@ struct pkv_handle_s {
     Shape shape{};
     std::string err;
     Plan plan;
+    // the image buffer of the previous plan, handed to the next one so that building its
+    // image reuses memory already mapped (the staged plan keeps no image)
+    std::vector<uint8_t> spare_image;
     void *planned_ws = nullptr;
     // Page-locked staging ring (PinnedIndexRing: depth 2; a set is rewritten only after
     // the copy out of it has completed, fenced by an event recorded after that copy).
@@ -167,6 +170,7 @@ static pkv_status stage_plan(pkv_handle_t h, Plan &plan, void *workspace, size_t
         h->pinned_bytes[set] = want;
     }
     std::memcpy(h->pinned[set], plan.image.data(), nbytes);
+    h->spare_image.swap(plan.image);
     e = cudaMemcpyAsync(workspace, h->pinned[set], nbytes, cudaMemcpyHostToDevice, st);
     if (e != cudaSuccess) return cuda_fail(h, e, "plan H2D");
     e = cudaEventRecord(h->fence[set], st);
@@ -191,10 +195,14 @@ extern "C" pkv_status pkv_plan(pkv_handle_t h, int mode, const int32_t *qo_indpt
     if (mode == PKV_MODE_MIXED && h->shape.max_prefill_rows < 0) return fail(h, PKV_ERR_INVALID, "no mixed config");
     std::string err;
     Plan plan;
+    plan.image.swap(h->spare_image);
     int rc = pkv::make_plan(h->shape, mode, qo_indptr, kv_indptr, kv_indices, last_page_len, batch, causal,
                             window_left, sm_scale, plan, err);
     h->planned_ws = nullptr;
-    if (rc) return fail(h, (pkv_status)rc, err);
+    if (rc) {
+        h->spare_image.swap(plan.image);
+        return fail(h, (pkv_status)rc, err);
+    }
     return stage_plan(h, plan, workspace, workspace_bytes, stream);
 }
 
@@ -532,8 +540,7 @@ extern "C" pkv_status pkv_decode_head_rows(pkv_handle_t h, const int32_t *kvp, c
     pkv::decode_split(h->shape, batch, kvp, lpl, qt.data(), ot.data(), window_left, dt, cta, mg, parts);
     const int ctas = dt.empty() ? 0 : (int)cta.size() - 1;
     if (ctas > *num_ctas) return fail(h, PKV_ERR_INVALID, "row buffer too small");
-    const std::vector<int32_t> pages(kvi, kvi + kvp[batch]);
-    const std::vector<int32_t> hr = pkv::decode_head_rows(h->shape, dt, cta, pages);
+    const std::vector<int32_t> hr = pkv::decode_head_rows(h->shape, dt, cta, kvi);
     std::copy(hr.begin(), hr.end(), rows);
     *num_ctas = ctas;
     return PKV_OK;
@@ -597,9 +604,13 @@ extern "C" pkv_status pkv_plan_dense(pkv_handle_t h, const int32_t *cu_q, const 
     if (!(sm_scale >= 0.f) || std::isinf(sm_scale)) return fail(h, PKV_ERR_INVALID, "sm_scale must be finite and >= 0");
     std::string err;
     Plan plan;
+    plan.image.swap(h->spare_image);
     int rc = pkv::make_dense_plan(h->shape, cu_q, cu_k, batch, causal, window_left, sm_scale, plan, err);
     h->planned_ws = nullptr;
-    if (rc) return fail(h, (pkv_status)rc, err);
+    if (rc) {
+        h->spare_image.swap(plan.image);
+        return fail(h, (pkv_status)rc, err);
+    }
     return stage_plan(h, plan, workspace, workspace_bytes, stream);
 }
 

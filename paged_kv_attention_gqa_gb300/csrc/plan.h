@@ -244,7 +244,7 @@ int mixed_layout(const int32_t *qo, const int32_t *kvp, const int32_t *kvi, cons
 // Rows of each decode CTA's first kDecodeHeadChunks chunks (its tiles' chunks in the order the
 // kernel walks them), -1 past the CTA's last chunk: int32[ctas][kDecodeHeadChunks].
 std::vector<int32_t> decode_head_rows(const Shape &s, const std::vector<DecodeTile> &tiles,
-                                      const std::vector<int32_t> &cta_ptr, const std::vector<int32_t> &pages);
+                                      const std::vector<int32_t> &cta_ptr, const int32_t *pages);
 void decode_split(const Shape &s, int rows, const int32_t *kvp, const int32_t *lpl, const int32_t *q_token,
                   const int32_t *out_token, int window_left, std::vector<DecodeTile> &tiles,
                   std::vector<int32_t> &cta_ptr, std::vector<MergeRow> &merges, int &num_partials,

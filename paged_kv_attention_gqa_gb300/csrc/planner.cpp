@@ -80,13 +80,18 @@ int validate_rows(const Shape &s, int mode, const int32_t *qo, const int32_t *kv
         err = "step has " + std::to_string(T) + " new tokens, above the handle's maximum " + std::to_string(tok_cap);
         return PKV_ERR_INVALID;
     }
-    for (int i = 0; i < kvp[batch]; ++i) {
-        if (kvi[i] < 0 || kvi[i] >= s.num_cache_pages) {
-            err = "page id " + std::to_string(kvi[i]) + " at paged_kv_indices[" + std::to_string(i) +
-                  "] outside [0, num_cache_pages=" + std::to_string(s.num_cache_pages) + ")";
-            return PKV_ERR_INVALID;
-        }
-    }
+    // every page id in [0, num_cache_pages): one unsigned compare per id, OR-ed together
+    // (a loop the compiler vectorises); the offending entry is looked up only on failure
+    const uint32_t num_pages = (uint32_t)s.num_cache_pages;
+    uint32_t bad = 0;
+    for (int i = 0; i < kvp[batch]; ++i) bad |= (uint32_t)(uint32_t)kvi[i] >= num_pages;
+    if (bad)
+        for (int i = 0; i < kvp[batch]; ++i)
+            if ((uint32_t)kvi[i] >= num_pages) {
+                err = "page id " + std::to_string(kvi[i]) + " at paged_kv_indices[" + std::to_string(i) +
+                      "] outside [0, num_cache_pages=" + std::to_string(s.num_cache_pages) + ")";
+                return PKV_ERR_INVALID;
+            }
     for (int r = 0; r < batch; ++r) {
         int np = kvp[r + 1] - kvp[r];
         int n = qo ? qo[r + 1] - qo[r] : 1;
@@ -241,8 +246,11 @@ void decode_split(const Shape &s, int rows, const int32_t *kvp, const int32_t *l
     const long long min_pages = (kMinKeysPerCta + P - 1) / P;
     long long per = std::max<long long>((W + cmax - 1) / cmax, min_pages);
     int ctas = (int)((W + per - 1) / per);
-    // Walk the rows' visible pages in order, cutting every `per` pages.
-    std::vector<std::vector<int>> row_tiles(rows);
+    // Walk the rows' visible pages in order, cutting every `per` pages.  The tiles of one row
+    // are consecutive: row r's are tiles [row_first[r], row_first[r] + row_count[r]).
+    std::vector<int> row_first(rows, 0), row_count(rows, 0);
+    tiles.reserve((size_t)rows + (size_t)ctas);
+    cta_ptr.reserve((size_t)ctas + 1);
     int r = 0, used = 0;  // pages of row r already assigned
     for (int c = 0; c < ctas; ++c) {
         long long budget = per;
@@ -261,7 +269,7 @@ void decode_split(const Shape &s, int rows, const int32_t *kvp, const int32_t *l
                 t.merge_row = -1;
                 t.append_token = -1;
                 t.pad[0] = t.pad[1] = 0;
-                row_tiles[r].push_back((int)tiles.size());
+                if (row_count[r]++ == 0) row_first[r] = (int)tiles.size();
                 tiles.push_back(t);
                 used += take;
                 budget -= take;
@@ -277,15 +285,15 @@ void decode_split(const Shape &s, int rows, const int32_t *kvp, const int32_t *l
     // the row's only token, the one its query comes from)
     if (mark_append)
         for (int rr = 0; rr < rows; ++rr)
-            if (!row_tiles[rr].empty()) tiles[row_tiles[rr].back()].append_token = q_token[rr];
+            if (row_count[rr]) tiles[row_first[rr] + row_count[rr] - 1].append_token = q_token[rr];
     for (int rr = 0; rr < rows; ++rr) {
-        if (row_tiles[rr].size() <= 1) continue;
+        if (row_count[rr] <= 1) continue;
         MergeRow m;
         m.out_token = out_token[rr];
         m.first = num_partials;
-        m.count = (int)row_tiles[rr].size();
+        m.count = row_count[rr];
         m.pad = 0;
-        for (int ti : row_tiles[rr]) {
+        for (int ti = row_first[rr]; ti < row_first[rr] + row_count[rr]; ++ti) {
             tiles[ti].partial = num_partials++;
             tiles[ti].merge_row = (int)merges.size();
         }
@@ -445,7 +453,7 @@ size_t workspace_bound(const Shape &s, int mode) {
 }
 
 std::vector<int32_t> decode_head_rows(const Shape &s, const std::vector<DecodeTile> &tiles,
-                                      const std::vector<int32_t> &cta_ptr, const std::vector<int32_t> &pages) {
+                                      const std::vector<int32_t> &cta_ptr, const int32_t *pages) {
     const int P = s.page_size;
     const int ctas = cta_ptr.empty() ? 0 : (int)cta_ptr.size() - 1;
     std::vector<int32_t> rows((size_t)ctas * kDecodeHeadChunks, -1);
@@ -469,13 +477,25 @@ static void put(std::vector<uint8_t> &img, size_t off, const T *src, size_t n) {
 }
 
 // Layout, device header and workspace image of a plan whose pieces are built.
+// dec_pages / pf_pages: the page lists of the two passes (dec_nnz / pf_nnz entries), read
+// from where they are (the caller's index array or the mixed layout), not copied first.
+// Reset `plan` to a fresh one, keeping the capacity of its image buffer: a handle hands the
+// buffer of its previous plan back in, so that building the image touches memory that is
+// already mapped instead of a new ~100 KB allocation per plan.
+static void reset_plan(Plan &plan) {
+    std::vector<uint8_t> keep;
+    keep.swap(plan.image);
+    plan = Plan();
+    plan.image.swap(keep);
+}
+
 static void finish_plan(const Shape &s, Plan &plan, int T, int window_left, const std::vector<int32_t> &app,
-                        const std::vector<int32_t> &dec_pages, const std::vector<int32_t> &pf_pages,
+                        const int32_t *dec_pages, int dec_nnz, const int32_t *pf_pages, int pf_nnz,
                         const std::vector<DecodeTile> &dtiles, std::vector<int32_t> &cta_ptr,
                         const std::vector<MergeRow> &merges, const std::vector<PrefillTile> &ptiles, int partials) {
     const int mode = plan.mode;
-    plan.dec_nnz = (int)dec_pages.size();
-    plan.pf_nnz = (int)pf_pages.size();
+    plan.dec_nnz = dec_nnz;
+    plan.pf_nnz = pf_nnz;
     plan.dec_tiles = (int)dtiles.size();
     plan.dec_ctas = dtiles.empty() ? 0 : (int)cta_ptr.size() - 1;
     plan.num_merge = (int)merges.size();
@@ -496,7 +516,7 @@ static void finish_plan(const Shape &s, Plan &plan, int T, int window_left, cons
         plan.lay = layout_for(s, T, plan.dec_nnz, plan.pf_nnz, plan.dec_tiles, plan.dec_ctas, plan.num_merge,
                               plan.pf_tiles, partials);
     }
-    plan.image.assign(plan.lay.int_bytes, 0);
+    plan.image.assign(plan.lay.int_bytes, 0);  // keeps the capacity a reused buffer already has
     PlanHeader hdr;
     hdr.err = 0;
     hdr.num_append = plan.num_append;
@@ -509,8 +529,8 @@ static void finish_plan(const Shape &s, Plan &plan, int T, int window_left, cons
     hdr.dense = mode == PKV_MODE_DENSE ? 1 : 0;
     put(plan.image, plan.lay.err, &hdr, 1);
     put(plan.image, plan.lay.append_rows, app.data(), app.size());
-    put(plan.image, plan.lay.dec_pages, dec_pages.data(), dec_pages.size());
-    put(plan.image, plan.lay.pf_pages, pf_pages.data(), pf_pages.size());
+    put(plan.image, plan.lay.dec_pages, dec_pages, (size_t)dec_nnz);
+    put(plan.image, plan.lay.pf_pages, pf_pages, (size_t)pf_nnz);
     put(plan.image, plan.lay.dec_tiles, dtiles.data(), dtiles.size());
     if (!cta_ptr.empty() && (plan.dec_ctas || s.graph_static)) {
         put(plan.image, plan.lay.dec_cta_ptr, cta_ptr.data(), cta_ptr.size());
@@ -526,7 +546,7 @@ int make_plan(const Shape &s, int mode, const int32_t *qo, const int32_t *kvp, c
               std::string &err) {
     int rc = validate_rows(s, mode, qo, kvp, kvi, lpl, batch, window_left, err, causal);
     if (rc) return rc;
-    plan = Plan();
+    reset_plan(plan);
     plan.mode = mode;
     plan.batch = batch;
     plan.causal = causal;
@@ -550,7 +570,9 @@ int make_plan(const Shape &s, int mode, const int32_t *qo, const int32_t *kvp, c
     std::vector<int32_t> cta_ptr;
     std::vector<MergeRow> merges;
     std::vector<PrefillTile> ptiles;
-    std::vector<int32_t> dec_pages, pf_pages;
+    MixedLayout m;  // mixed plans: outlives the branch, finish_plan reads its page list
+    const int32_t *dec_pages = nullptr, *pf_pages = nullptr;  // the passes' page lists
+    int dec_nnz = 0, pf_nnz = 0;
     int partials = 0;
 
     if (mode == PKV_MODE_DECODE) {
@@ -558,15 +580,16 @@ int make_plan(const Shape &s, int mode, const int32_t *qo, const int32_t *kvp, c
         for (int r = 0; r < batch; ++r) qt[r] = ot[r] = r;
         decode_split(s, batch, kvp, lpl, qt.data(), ot.data(), window_left, dtiles, cta_ptr, merges, partials, 0,
                      plan.num_append > 0);
-        dec_pages.assign(kvi, kvi + kvp[batch]);
+        dec_pages = kvi;
+        dec_nnz = kvp[batch];
         plan.dec_rows = batch;
     } else if (mode == PKV_MODE_PREFILL) {
         std::vector<int> rows(batch);
         for (int r = 0; r < batch; ++r) rows[r] = r;
         prefill_tiles(s, rows, qo, qo, kvp, lpl, causal, window_left, ptiles);
-        pf_pages.assign(kvi, kvi + kvp[batch]);
+        pf_pages = kvi;
+        pf_nnz = kvp[batch];
     } else if (mode == PKV_MODE_MIXED) {
-        MixedLayout m;
         rc = mixed_layout(qo, kvp, kvi, lpl, batch, s.max_prefill_rows, s.sink_page, m, err);
         if (rc) return rc;
         if (m.dec_kv_indices.size() > 0 && s.sink_page >= s.num_cache_pages) {
@@ -587,7 +610,8 @@ int make_plan(const Shape &s, int mode, const int32_t *qo, const int32_t *kvp, c
             qbeg[r] = m.perm[m.pf_qo_indptr[k]];
         }
         prefill_tiles(s, rows, qbeg.data(), qo, kvp, lpl, causal, window_left, ptiles);
-        pf_pages.assign(kvi, kvi + kvp[batch]);
+        pf_pages = kvi;
+        pf_nnz = kvp[batch];
         // Decode pass over every row: a decode row attends its own pages, any other row
         // one token of the sink page; the latter's result is dropped (out_token -1).  The
         // two passes run concurrently: the decode pass gets the SMs its bytes need, the
@@ -596,13 +620,15 @@ int make_plan(const Shape &s, int mode, const int32_t *qo, const int32_t *kvp, c
                      m.dec_out_token.data(), window_left, dtiles, cta_ptr, merges, partials,
                      mixed_decode_ctas(s, batch, m.dec_kv_indptr.data(), m.dec_last_page_len.data(), window_left,
                                        ptiles));
-        dec_pages = m.dec_kv_indices;
+        dec_pages = m.dec_kv_indices.data();
+        dec_nnz = (int)m.dec_kv_indices.size();
         plan.dec_rows = batch;
     } else {
         err = "unknown plan mode";
         return PKV_ERR_INVALID;
     }
-    finish_plan(s, plan, T, window_left, app, dec_pages, pf_pages, dtiles, cta_ptr, merges, ptiles, partials);
+    finish_plan(s, plan, T, window_left, app, dec_pages, dec_nnz, pf_pages, pf_nnz, dtiles, cta_ptr, merges, ptiles,
+                partials);
     return PKV_OK;
 }
 
@@ -641,7 +667,7 @@ int make_dense_plan(const Shape &s, const int32_t *cu_q, const int32_t *cu_k, in
         err = "dense plan has " + std::to_string(cu_q[batch]) + " queries, above max_total_tokens";
         return PKV_ERR_INVALID;
     }
-    plan = Plan();
+    reset_plan(plan);
     plan.mode = PKV_MODE_DENSE;
     plan.batch = batch;
     plan.causal = causal;
@@ -652,7 +678,7 @@ int make_dense_plan(const Shape &s, const int32_t *cu_q, const int32_t *cu_k, in
     std::vector<PrefillTile> ptiles;
     prefill_tiles_rows(s, rows, causal, window_left, ptiles, true);
     std::vector<int32_t> none, cta;
-    finish_plan(s, plan, plan.num_tokens, window_left, none, none, none, {}, cta, {}, ptiles, 0);
+    finish_plan(s, plan, plan.num_tokens, window_left, none, nullptr, 0, nullptr, 0, {}, cta, {}, ptiles, 0);
     return PKV_OK;
 }
 
