@@ -22,7 +22,8 @@
 //    lane).  The two groups take turns (a token passed through two mbarriers): while one
 //    group turns S into P the tensor pipe runs the other tile's MMAs -- PV1_{j-1} and S1_j
 //    under the softmax of S0_j, PV0_j and S0_{j+1} under that of S1_j -- and neither group
-//    shares the SM sub-partitions with the other.
+//    shares the SM sub-partitions with the other during its exp pass.  At head_dim 64 a group
+//    passes the turn on once it has loaded S, so the other group's load overlaps its exp pass.
 //  * Each S_X overwrites the columns that PV_X of the previous tile read P from, so S_X(j+1)
 //    is issued once PV_X(j) has completed; the other tile's MMAs keep the pipe busy meanwhile.
 //  * The running maximum moves (and O is rescaled in tensor memory) only when it grows by more
@@ -327,6 +328,12 @@ __global__ void __launch_bounds__(kPpThreads, 1)
                 tmem_ld32(Sx + 64, r2);
                 tmem_ld32(Sx + 96, r3);
                 tmem_wait_ld();
+                if constexpr (D == 64) {
+                    // head_dim 64 (half the MMA work per tile, so the softmax weighs more): the
+                    // other group may start as soon as this one holds its S in registers
+                    __syncwarp();
+                    if (two && lane == 0) mbar_arrive(&turn[1 - x]);
+                }
                 float sv[kPpKeys];
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
@@ -390,8 +397,10 @@ __global__ void __launch_bounds__(kPpThreads, 1)
                 float u0, u1;
                 f2_split(fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3])), u0, u1);
                 l_run = l_run * alpha + (u0 + u1);
-                __syncwarp();
-                if (two && lane == 0) mbar_arrive(&turn[1 - x]);  // the other group's turn
+                if constexpr (D != 64) {
+                    __syncwarp();
+                    if (two && lane == 0) mbar_arrive(&turn[1 - x]);  // the other group's turn
+                }
                 tmem_wait_st();
                 if (warp_grow) {
                     // O holds P_0..P_{j-1} V: wait for the last of those MMAs, then scale O rows

@@ -19,7 +19,8 @@ Checked under many random schedules:
     tiles') completed; the softmax reads S_X(j) only after it completed; PV_X(j) is issued only
     after P_X(j) was written and V_j landed (and, on the last tile, after its tail rows were
     zeroed); O_X is rescaled only while no PV_X is in flight; the epilogue reads O_X after all PV_X;
-  * the two softmax groups never run their main passes at the same time (the turns hold);
+  * the two softmax groups never run their main passes at the same time (the turns hold); with
+    the head_dim-64 schedule (the turn passed on once S is loaded) their S loads never overlap;
   * every actor finishes (no deadlock), with one query tile or two.
 Planted mistakes -- S issued without waiting for the previous PV, a stage released after one
 warp's MMAs only, no turns, warp 10 not waiting for the tail rows -- are caught."""
@@ -48,9 +49,10 @@ class Barrier:
 class Sim:
     NS = 4
 
-    def __init__(self, nt, two, seed, plant=None, tail=True):
+    def __init__(self, nt, two, seed, plant=None, tail=True, early_turn=False):
         self.rng = random.Random(seed)
         self.nt, self.two, self.plant, self.tail = nt, two, plant, tail
+        self.early_turn = early_turn  # head_dim 64: the turn passes once S is loaded
         self.nq = 2 if two else 1
         self.t, self.seq, self.q = 0, 0, []
         B = Barrier
@@ -186,10 +188,17 @@ class Sim:
             assert self.s_cpl[x][j] <= self.t, f"softmax {x} read S({j}) before it completed"
             self.in_main[x] += 1
             assert self.in_main[1 - x] == 0, f"both softmax groups in their main pass at tile {j}"
-            yield ("delay", self.rng.randint(50, 900))
-            self.in_main[x] -= 1
-            if self.two and self.plant != "no_turn":
-                self.turn[1 - x].arrive(self)
+            if self.early_turn:
+                yield ("delay", self.rng.randint(10, 200))  # the S load
+                self.in_main[x] -= 1
+                if self.two and self.plant != "no_turn":
+                    self.turn[1 - x].arrive(self)
+                yield ("delay", self.rng.randint(50, 800))  # max and exp pass
+            else:
+                yield ("delay", self.rng.randint(50, 900))
+                self.in_main[x] -= 1
+                if self.two and self.plant != "no_turn":
+                    self.turn[1 - x].arrive(self)
             if j > 0 and self.rng.random() < 0.3:  # the running max grew: rescale O_X
                 yield ("wait", self.pv_done[x], j - 1)
                 inflight = [i for i, t in self.pv_cpl[x].items() if t > self.t]
@@ -213,19 +222,21 @@ class Sim:
         assert self.finished == len(actors), f"deadlock: {self.finished} of {len(actors)} actors finished"
 
 
+@pytest.mark.parametrize("early_turn", [False, True])
 @pytest.mark.parametrize("two", [False, True])
 @pytest.mark.parametrize("nt", [0, 1, 2, 3, 4, 5, 8, 13])
-def test_pair_barrier_protocol_is_sound(nt, two):
+def test_pair_barrier_protocol_is_sound(nt, two, early_turn):
     for seed in range(120):
-        Sim(nt, two, seed * 1000 + nt, tail=bool(seed & 1)).run()
+        Sim(nt, two, seed * 1000 + nt, tail=bool(seed & 1), early_turn=early_turn).run()
 
 
+@pytest.mark.parametrize("early_turn", [False, True])
 @pytest.mark.parametrize("plant", ["no_pv_wait", "single_release", "no_turn", "no_tail_wait"])
-def test_pair_model_catches_a_broken_protocol(plant):
+def test_pair_model_catches_a_broken_protocol(plant, early_turn):
     caught = 0
     for seed in range(200):
         try:
-            Sim(8, True, seed, plant=plant, tail=True).run()
+            Sim(8, True, seed, plant=plant, tail=True, early_turn=early_turn).run()
         except AssertionError:
             caught += 1
     assert caught > 0
