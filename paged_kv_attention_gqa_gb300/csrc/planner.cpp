@@ -84,7 +84,7 @@ int validate_rows(const Shape &s, int mode, const int32_t *qo, const int32_t *kv
     // (a loop the compiler vectorises); the offending entry is looked up only on failure
     const uint32_t num_pages = (uint32_t)s.num_cache_pages;
     uint32_t bad = 0;
-    for (int i = 0; i < kvp[batch]; ++i) bad |= (uint32_t)(uint32_t)kvi[i] >= num_pages;
+    for (int i = 0; i < kvp[batch]; ++i) bad |= (uint32_t)kvi[i] >= num_pages;
     if (bad)
         for (int i = 0; i < kvp[batch]; ++i)
             if ((uint32_t)kvi[i] >= num_pages) {
@@ -476,9 +476,6 @@ static void put(std::vector<uint8_t> &img, size_t off, const T *src, size_t n) {
     if (n) std::memcpy(img.data() + off, src, n * sizeof(T));
 }
 
-// Layout, device header and workspace image of a plan whose pieces are built.
-// dec_pages / pf_pages: the page lists of the two passes (dec_nnz / pf_nnz entries), read
-// from where they are (the caller's index array or the mixed layout), not copied first.
 // Reset `plan` to a fresh one, keeping the capacity of its image buffer: a handle hands the
 // buffer of its previous plan back in, so that building the image touches memory that is
 // already mapped instead of a new ~100 KB allocation per plan.
@@ -489,6 +486,9 @@ static void reset_plan(Plan &plan) {
     plan.image.swap(keep);
 }
 
+// Layout, device header and workspace image of a plan whose pieces are built.
+// dec_pages / pf_pages: the page lists of the two passes (dec_nnz / pf_nnz entries), read
+// from where they are (the caller's index array or the mixed layout), not copied first.
 static void finish_plan(const Shape &s, Plan &plan, int T, int window_left, const std::vector<int32_t> &app,
                         const int32_t *dec_pages, int dec_nnz, const int32_t *pf_pages, int pf_nnz,
                         const std::vector<DecodeTile> &dtiles, std::vector<int32_t> &cta_ptr,
