@@ -13,7 +13,8 @@
 //  * warp 4 loads Q once and streams the 128-key K tiles, warp 5 the V tiles (TMA boxes of 16 or 8
 //    slots of the kv head, 64-column quarters, 128-byte swizzle; one lane per box, its page looked
 //    up a tile ahead), one stage each (a tile of 128 keys x 256 columns is 64 KB); the K stage is
-//    refilled quarter by quarter as S(j)'s k-steps release them;
+//    refilled by 64-column quarter as S(j)'s k-steps release them, the V stage by quarter of 32
+//    keys as PV(j)'s k-steps release those;
 //  * tensor memory holds two S buffers of 128 fp32 columns (P written over each as bf16) and O
 //    (256 fp32 columns).  Warp 6 issues S(j) = Q K_j^T (N = 128: both operands in shared memory at
 //    the full MMA rate) into buffer j % 2 once PV(j-2), which read P(j-2) from it, completed; warp
@@ -63,17 +64,19 @@ __global__ void __launch_bounds__(kPwThreads, 1)
     constexpr int BQ = kPrefillRowsPerTile / G;          // tokens per query tile
     constexpr uint32_t Q_TX = (uint32_t)BQ * G * D * 2;  // rows BQ*G..127 stay unused
     constexpr int PSTEPS = kPwKeys / 16;                 // k-steps of O += P V
+    static_assert(PSTEPS == 8, "two PV k-steps per 32-key quarter of V");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::BAR_OFF);
     // K / V stages, S / P buffers and PV completions: once per K/V tile (q_full, o_final once)
     // The K stage is filled and released by 64-column quarter: S(j)'s k-steps read the quarters in
     // turn, so quarter q of K(j+1) is requested once the MMAs reading quarter q of K(j) completed.
+    // The V stage likewise by quarter of 32 keys: PV(j)'s k-steps read its keys in order.
     uint64_t *q_full = bars + 0;
     uint64_t *k_full = bars + 1;    // [4] a quarter of K(j) landed
     uint64_t *k_empty = bars + 5;   // [4] the S MMAs reading a quarter of K(j) completed
-    uint64_t *v_full = bars + 9;
-    uint64_t *v_empty = bars + 10;  // the PV MMAs reading the V stage completed
+    uint64_t *v_full = bars + 19;   // [4] a quarter (32 keys) of V(j) landed
+    uint64_t *v_empty = bars + 23;  // [4] the PV MMAs reading a quarter of V(j) completed
     uint64_t *s_full = bars + 11;   // [2] S(j) in buffer j % 2
     uint64_t *p_full = bars + 13;   // [2] P(j) written over buffer j % 2 (and O rescaled if it had to be)
     uint64_t *pv_done = bars + 15;  // [2] PV(j) completed, counted on buffer j % 2
@@ -98,8 +101,10 @@ __global__ void __launch_bounds__(kPwThreads, 1)
             mbar_init(&k_full[q], 1);
             mbar_init(&k_empty[q], 1);
         }
-        mbar_init(v_full, 1);
-        mbar_init(v_empty, 1);
+        for (int q = 0; q < 4; ++q) {
+            mbar_init(&v_full[q], 1);
+            mbar_init(&v_empty[q], 1);
+        }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&s_full[b], 1);
             mbar_init(&p_full[b], 4);
@@ -167,14 +172,22 @@ __global__ void __launch_bounds__(kPwThreads, 1)
         bool ok = true;
         for (int j = 0; j < nt && ok; ++j) {
             if (kv) {
-                // the PV MMAs that read the stage's previous tile must have completed
-                if (j > 0 && !mbar_wait(v_empty, (j - 1) & 1, err, kErrWaitEmpty)) break;
-                if (lane == 0) mbar_arrive_expect_tx(v_full, L::KV_TILE);
-                __syncwarp();
-                if (lane < NB) {
+                // key quarter kq (32 keys: boxes kq * NB / 4 .. of NB / 4 lanes), each box with its
+                // four 64-column quarters
+                for (int kq = 0; kq < 4; ++kq) {
+                    // the PV MMAs that read this key quarter of the previous tile must have completed
+                    if (j > 0 && !mbar_wait(&v_empty[kq], (j - 1) & 1, err, kErrWaitEmpty)) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0) mbar_arrive_expect_tx(&v_full[kq], L::KV_TILE / 4);
+                    __syncwarp();
+                    if (lane < NB && lane / (NB / 4) == kq) {
 #pragma unroll
-                    for (int h = 0; h < QUARTERS; ++h)
-                        tma_load_3d(stage + h * L::KV_QUARTER + lane * R * 128, map, v_full, h * 64, row, t.kv_head);
+                        for (int h = 0; h < QUARTERS; ++h)
+                            tma_load_3d(stage + h * L::KV_QUARTER + lane * R * 128, map, &v_full[kq], h * 64, row,
+                                        t.kv_head);
+                    }
                 }
             } else {
                 for (int h = 0; h < QUARTERS; ++h) {
@@ -226,34 +239,44 @@ __global__ void __launch_bounds__(kPwThreads, 1)
         bool ok = true;
         for (int j = 0; j < nt && ok; ++j) {
             const int b = j & 1;
-            ok = mbar_wait(v_full, j & 1, err, kErrWaitFull);
-            if (!ok) break;
-            // V rows of the row's last page past its end (poisoned or stale slots: their P is 0,
-            // but 0 * NaN would poison O) are zeroed first (the last tile: keys never reach past
-            // the row's end)
-            const int key0 = (kt0 + j) * kPwKeys;
-            const int zb = max(tail_begin, key0), ze = min(tail_end, key0 + kPwKeys);
-            if (zb < ze) {
-                uint8_t *vs = sm + L::V_OFF;
-                const int nz = (ze - zb) * (D / 8);
-                for (int e = lane; e < nz; e += 32) {
-                    const int k = zb - key0 + e / (D / 8);
-                    const int chunk = e % (D / 8);
-                    *reinterpret_cast<uint4 *>(vs + (chunk >> 3) * L::KV_QUARTER + swz128(k, chunk & 7)) =
-                        make_uint4(0, 0, 0, 0);
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-            }
             ok = mbar_wait(&p_full[b], (j >> 1) & 1, err, kErrWaitFull);
             if (!ok) break;
-            tc_fence_after();
+            const int key0 = (kt0 + j) * kPwKeys;
+#pragma unroll 1
+            for (int kq = 0; kq < 4 && ok; ++kq) {
+                ok = mbar_wait(&v_full[kq], j & 1, err, kErrWaitFull);
+                if (!ok) break;
+                // V rows of the row's last page past its end (poisoned or stale slots: their P is
+                // 0, but 0 * NaN would poison O) are zeroed before the MMAs read them (the last
+                // tile: keys never reach past the row's end), quarter by quarter
+                const int qb = key0 + kq * (kPwKeys / 4);
+                const int zb = max(tail_begin, qb), ze = min(tail_end, qb + kPwKeys / 4);
+                if (zb < ze) {
+                    uint8_t *vs = sm + L::V_OFF;
+                    const int nz = (ze - zb) * (D / 8);
+                    for (int e = lane; e < nz; e += 32) {
+                        const int k = zb - key0 + e / (D / 8);
+                        const int chunk = e % (D / 8);
+                        *reinterpret_cast<uint4 *>(vs + (chunk >> 3) * L::KV_QUARTER + swz128(k, chunk & 7)) =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
+                tc_fence_after();
 #pragma unroll
-            for (int kk = 0; kk < PSTEPS; ++kk)  // 16 keys = 16 rows of 128 bytes per k-step
-                mma_ts_elect(O_col, tmem + 128u * (uint32_t)b + kk * 8, pw_desc(dV, kk * 2048), ID_O,
-                             (j > 0 || kk > 0) ? 1u : 0u);
+                for (int kk = 2 * kq; kk < 2 * kq + 2; ++kk)  // 16 keys = 16 rows of 128 bytes per k-step
+                    mma_ts_elect(O_col, tmem + 128u * (uint32_t)b + kk * 8, pw_desc(dV, kk * 2048), ID_O,
+                                 (j > 0 || kk > 0) ? 1u : 0u);
+                mma_commit_elect(&v_empty[kq]);  // this key quarter of V_j frees once these MMAs completed
+            }
+            if (!ok) {
+                // let the MMAs already issued finish before the tensor memory is released
+                mma_commit_elect(&pv_done[b]);
+                mbar_wait(&pv_done[b], (j >> 1) & 1, err, kErrWaitFull);
+                break;
+            }
             mma_commit_elect(&pv_done[b]);
-            mma_commit_elect(v_empty);  // V_j's stage frees once these MMAs completed
             if (j == nt - 1) mma_commit_elect(o_final);
         }
         if (nt == 0 && lane == 0) mma_commit(o_final);  // no MMA: arrives at once

@@ -6,7 +6,9 @@ does.
 
 The kernel's barriers: q_full; k_full[4] / k_empty[4] (one K stage, filled and released by 64-column
 quarter: S(j)'s k-steps read the quarters in turn, so quarter q of K(j+1) is requested as soon as
-the MMAs reading quarter q of K(j) completed); v_full / v_empty (one V stage);
+the MMAs reading quarter q of K(j) completed); v_full[4] / v_empty[4] (one V stage, filled and
+released by quarter of 32 keys: PV(j)'s k-steps read the key quarters in turn, so quarter q of
+V(j+1) is requested as soon as the MMAs reading quarter q of V(j) completed);
 s_full[2] (S(j) done in tensor-memory buffer j % 2), p_full[2] (the four softmax warps wrote P(j)
 over that buffer), pv_done[2] (PV(j) done, counted per buffer), o_final. A commit makes its barrier
 arrive once every MMA its own warp issued before it has completed.
@@ -17,12 +19,14 @@ Checked under many random schedules:
   * no hazard: S(j) is issued only after K_j landed and after PV(j-2), which reads P(j-2) from the
     same buffer, completed; a stage is refilled only after the MMAs reading it completed; the
     softmax reads S(j) only after it completed; PV(j) is issued only after P(j) was written by all
-    four warps and V_j landed (and, on the last tile, after its tail rows were zeroed); O is
+    four warps, and each key quarter of it only after that quarter of V_j landed (and, on the
+    last tile, after its tail rows were zeroed); O is
     rescaled only while no PV is in flight; the epilogue reads O after all PVs;
   * every actor finishes (no deadlock).
 Planted mistakes -- S(j) issued without waiting for PV(j-2), one pv_done barrier for both buffers
 (waited two phases back), PV issued without waiting for P, the tail rows not zeroed first, every K
-quarter refilled on the first quarter's release -- are caught."""
+quarter refilled on the first quarter's release, every V quarter refilled on the first quarter's
+release -- are caught."""
 import heapq
 import random
 
@@ -40,7 +44,8 @@ class Sim:
         self.q_full = B("q_full", 1)
         self.k_full = [B(f"k_full{q}", 1) for q in range(4)]
         self.k_empty = [B(f"k_empty{q}", 1) for q in range(4)]
-        self.v_full, self.v_empty = B("v_full", 1), B("v_empty", 1)
+        self.v_full = [B(f"v_full{q}", 1) for q in range(4)]
+        self.v_empty = [B(f"v_empty{q}", 1) for q in range(4)]
         self.s_full = [B(f"s_full{b}", 1) for b in range(2)]
         self.p_full = [B(f"p_full{b}", 4) for b in range(2)]
         self.pv_done = [B(f"pv_done{b}", 1) for b in range(2)]
@@ -92,13 +97,14 @@ class Sim:
     def producer(self, kv):
         if kv == 0:
             self.q_full.arrive(self)
-        parts = range(4) if kv == 0 else [None]
         for j in range(self.nt):
-            for q in parts:
-                full = self.k_full[q] if kv == 0 else self.v_full
-                empty = self.k_empty[q if self.plant != "k_single_release" else 0] if kv == 0 else self.v_empty
-                key = ("K", j, q) if kv == 0 else ("V", j)
-                prev = ("K", j - 1, q) if kv == 0 else ("V", j - 1)
+            for q in range(4):
+                if kv == 0:
+                    full, empty = self.k_full[q], self.k_empty[q if self.plant != "k_single_release" else 0]
+                else:
+                    full, empty = self.v_full[q], self.v_empty[q if self.plant != "v_single_release" else 0]
+                key = ("K" if kv == 0 else "V", j, q)
+                prev = ("K" if kv == 0 else "V", j - 1, q)
                 if j > 0:
                     yield ("wait", empty, j - 1)
                     late = [c for c in self.readers.get(prev, []) if c > self.t]
@@ -130,22 +136,27 @@ class Sim:
 
     def pv_issuer(self):
         for j in range(self.nt):
-            yield ("wait", self.v_full, j)
-            if self.tail and j == self.nt - 1 and self.plant != "no_tail":
-                yield ("delay", self.rng.randint(5, 3000))  # zero the V rows past the row's end
-                self.tail_zeroed = self.t
             if self.plant != "no_p_wait":
                 yield ("wait", self.p_full[j % 2], j // 2)
             pw = self.p_written.get(j, [])
             assert len(pw) == 4 and max(pw) <= self.t, f"PV({j}) before P({j}) written"
-            assert self.land.get(("V", j), 1 << 60) <= self.t, f"PV({j}) before V_{j} landed"
-            if self.tail and j == self.nt - 1:
-                assert self.tail_zeroed is not None and self.tail_zeroed <= self.t, f"PV({j}) before the tail was zeroed"
-            self.pv_cpl[j] = self.issue("pv", ("V", j))
+            done = 0
+            for q in range(4):  # the k-steps of key quarter q, then its release
+                yield ("wait", self.v_full[q], j)
+                if self.tail and j == self.nt - 1 and self.plant != "no_tail":
+                    yield ("delay", self.rng.randint(5, 1000))  # zero this quarter's V rows past the row's end
+                    self.tail_zeroed = self.t
+                assert self.land.get(("V", j, q), 1 << 60) <= self.t, f"PV({j}) quarter {q} before it landed"
+                if self.tail and j == self.nt - 1:
+                    assert self.tail_zeroed is not None and self.tail_zeroed <= self.t, \
+                        f"PV({j}) before the tail was zeroed"
+                done = max(done, self.issue("pv", ("V", j, q)))
+                self.commit("pv", self.v_empty[q])
+                yield ("delay", self.rng.randint(1, 40))
+            self.pv_cpl[j] = done
             self.commit("pv", self.pv_done[j % 2])
             if self.plant == "single_pv_barrier":
                 self.commit("pv", self.pv_one)
-            self.commit("pv", self.v_empty)
             if j == self.nt - 1:
                 self.commit("pv", self.o_final)
             yield ("delay", self.rng.randint(1, 40))
@@ -184,7 +195,8 @@ def test_wide_barrier_protocol_is_sound(nt):
         Sim(nt, seed * 1000 + nt, tail=bool(seed & 1)).run()
 
 
-@pytest.mark.parametrize("plant", ["no_buf_wait", "single_pv_barrier", "no_p_wait", "no_tail", "k_single_release"])
+@pytest.mark.parametrize("plant", ["no_buf_wait", "single_pv_barrier", "no_p_wait", "no_tail", "k_single_release",
+                                   "v_single_release"])
 def test_wide_model_catches_a_broken_protocol(plant):
     caught = 0
     for seed in range(200):
