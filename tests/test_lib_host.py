@@ -254,6 +254,24 @@ def test_plan_validation(lib, case, status):
         assert "needs" in msg and re.search(r"\d{4,}", msg)
 
 
+@pytest.mark.parametrize("bad_at,bad_id", [(0, 100), (17, -1), (33, 2**31 - 1), (5, -2**31)])
+def test_plan_names_the_first_page_id_outside_the_cache(lib, bad_at, bad_id):
+    """Page ids are range-checked all at once and the offending entry is looked up afterwards:
+    the error names the first id outside [0, num_cache_pages) and its index, wherever it sits
+    (first, middle or last entry, negative or past the pool), and a second bad id further on
+    does not change which one is named."""
+    h = _handle(num_cache_pages=100, max_num_pages=100, max_prefill_rows=1, sink_page=99)
+    kvi = list(range(40, 74))  # 34 valid ids: rows of 20 and 14 pages
+    kvi[bad_at] = bad_id
+    if bad_at + 1 < len(kvi):
+        kvi[-1] = 1000  # a later bad id
+    st, msg = _plan_status(h, B.MODE_PREFILL, ([0, 1, 4], [0, 20, 34], kvi, [3, 16]))
+    assert st == B.ERR_INVALID, (st, msg)
+    assert f"page id {bad_id} at paged_kv_indices[{bad_at}]" in msg, msg
+    ok = list(range(40, 74))
+    assert _plan_status(h, B.MODE_PREFILL, ([0, 1, 4], [0, 20, 34], ok, [3, 16]), ws_bytes=1024)[0] == B.ERR_WORKSPACE
+
+
 def test_workspace_bound_holds(lib):
     for name in ["tiny", "batch", "prefill", "mixed", "long"]:
         pb = wl.WORKLOADS[name]()
