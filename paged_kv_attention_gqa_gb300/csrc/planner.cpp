@@ -307,62 +307,69 @@ struct PrefillRow {
     int kv_base;  // paged: offset of the first page in the page list; dense: first key row
 };
 
-// Work tiles of the rows' new tokens into `out` (cleared first).
+// Work tiles of the rows' new tokens into `out` (cleared first), in dispatch order: the q-tiles of
+// one (row, kv head) next to each other, so the CTAs in flight together stream the same K/V pages
+// and share them in L2; groups longest first (by their longest tile), and longest first inside a
+// group, approximating LPT.  Every kv head of a row sees the same key ranges, so the order is
+// built directly: rows by their longest tile (ties by page offset, which differs between rows),
+// the row's kv heads in turn, and each head's q-tiles longest first (ties in token order).
 static void prefill_tiles_rows(const Shape &s, const std::vector<PrefillRow> &rows, int causal, int window_left,
                                std::vector<PrefillTile> &out, bool dense = false) {
     // tokens per work tile: one query tile of 128 / g tokens, or two on the paired kernel
     const int BQ = s.pf_tile_tokens(dense);
     out.clear();
-    // group_len[i]: the longest key range of tile i's group (its row and kv head); every kv head
-    // of a row sees the same key ranges, so a group's longest range is its row's
-    std::vector<int> group_len;
+    struct RowTiles {
+        int len_max;   // the row's longest key range
+        int kv_base;
+        int first, n;  // its q-tiles in qtiles
+    };
+    std::vector<PrefillTile> qtiles;  // one per (row, q-tile), kv head 0
+    std::vector<RowTiles> rts;
     for (const PrefillRow &pr : rows) {
         const int n = pr.n, L = pr.L;
         if (n <= 0) continue;
         // causal 2 (context-only): the row's pages hold the context; its queries follow it
         const int c = causal == 2 ? L : L - n;
-        const size_t row_first = out.size();
-        int row_len_max = 0;
+        RowTiles rt{0, pr.kv_base, (int)qtiles.size(), 0};
         for (int t0 = 0; t0 < n; t0 += BQ) {
             int nq = std::min(BQ, n - t0);
             int p0 = c + t0, p1 = c + t0 + nq - 1;
             int kb = window_left >= 0 ? std::max(0, p0 - window_left) : 0;
             int ke = causal == 1 ? p1 + 1 : L;
             if (ke <= kb) kb = ke = 0;  // no query of the tile sees a key: zeros, lse -inf
-            row_len_max = std::max(row_len_max, ke - kb);
-            for (int hk = 0; hk < s.num_kv_heads; ++hk) {
-                PrefillTile t;
-                t.q_begin = pr.q_begin + t0;
-                t.n_q = nq;
-                t.pos0 = p0;
-                t.length = L;
-                t.kv_base = pr.kv_base;
-                t.kv_head = hk;
-                t.key_begin = kb;
-                t.key_end = ke;
-                out.push_back(t);
-            }
+            PrefillTile t;
+            t.q_begin = pr.q_begin + t0;
+            t.n_q = nq;
+            t.pos0 = p0;
+            t.length = L;
+            t.kv_base = pr.kv_base;
+            t.kv_head = 0;
+            t.key_begin = kb;
+            t.key_end = ke;
+            qtiles.push_back(t);
+            rt.len_max = std::max(rt.len_max, ke - kb);
+            ++rt.n;
         }
-        group_len.resize(out.size(), 0);
-        for (size_t i = row_first; i < out.size(); ++i) group_len[i] = row_len_max;
+        rts.push_back(rt);
     }
-    // Dispatch order: the q-tiles of one (row, kv head) next to each other, so the CTAs in
-    // flight together stream the same K/V pages and share them in L2; groups longest first
-    // (by their longest tile), and longest first inside a group, approximating LPT.  The sort
-    // keys are plain integers computed above (a stable sort of tile indices, then a gather).
-    std::vector<int> order(out.size());
-    for (size_t i = 0; i < order.size(); ++i) order[i] = (int)i;
-    std::stable_sort(order.begin(), order.end(), [&](int ia, int ib) {
-        const PrefillTile &a = out[ia], &b = out[ib];
-        if (group_len[ia] != group_len[ib]) return group_len[ia] > group_len[ib];
-        if (a.kv_base != b.kv_base) return a.kv_base < b.kv_base;
-        if (a.kv_head != b.kv_head) return a.kv_head < b.kv_head;
-        return (a.key_end - a.key_begin) > (b.key_end - b.key_begin);
+    std::stable_sort(rts.begin(), rts.end(), [](const RowTiles &a, const RowTiles &b) {
+        if (a.len_max != b.len_max) return a.len_max > b.len_max;
+        return a.kv_base < b.kv_base;
     });
-    std::vector<PrefillTile> sorted;
-    sorted.reserve(out.size());
-    for (int i : order) sorted.push_back(out[i]);
-    out.swap(sorted);
+    out.reserve(qtiles.size() * (size_t)s.num_kv_heads);
+    std::vector<int> ord;
+    for (const RowTiles &rt : rts) {
+        ord.resize(rt.n);
+        for (int i = 0; i < rt.n; ++i) ord[i] = rt.first + i;
+        std::stable_sort(ord.begin(), ord.end(), [&](int a, int b) {
+            return (qtiles[a].key_end - qtiles[a].key_begin) > (qtiles[b].key_end - qtiles[b].key_begin);
+        });
+        for (int hk = 0; hk < s.num_kv_heads; ++hk)
+            for (int i : ord) {
+                out.push_back(qtiles[i]);
+                out.back().kv_head = hk;
+            }
+    }
 }
 
 static void prefill_tiles(const Shape &s, const std::vector<int> &rows, const int32_t *q_begin_of_row,
