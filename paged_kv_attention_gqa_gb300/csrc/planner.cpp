@@ -187,10 +187,15 @@ int mixed_layout(const int32_t *qo, const int32_t *kvp, const int32_t *kvi, cons
     m.dec_last_page_len.clear();
     m.dec_q_token.clear();
     m.dec_out_token.clear();
+    m.dec_kv_indptr.reserve((size_t)batch + 1);
+    m.dec_kv_indices.reserve((size_t)kvp[batch] + (size_t)batch);
+    m.dec_last_page_len.reserve(batch);
+    m.dec_q_token.reserve(batch);
+    m.dec_out_token.reserve(batch);
     for (int r = 0; r < batch; ++r) {
         int n = qo[r + 1] - qo[r];
         if (n == 1) {
-            for (int i = kvp[r]; i < kvp[r + 1]; ++i) m.dec_kv_indices.push_back(kvi[i]);
+            m.dec_kv_indices.insert(m.dec_kv_indices.end(), kvi + kvp[r], kvi + kvp[r + 1]);
             m.dec_last_page_len.push_back(lpl[r]);
             m.dec_out_token.push_back(qo[r]);
         } else {
